@@ -1,0 +1,199 @@
+"""GB300-native two-stage draft LM head: Python binding of liblmhead.so.
+
+Argument marshalling only: every step of the head runs in the library's CUDA
+kernels; PyTorch supplies device memory and streams. Tensors are CUDA,
+contiguous, row-major; bf16 tensors may be torch.bfloat16 or 16-bit integer
+views of bf16 bits. Names follow the C ABI (include/lmhead.h) without the
+`lmhead_` prefix.
+
+    ids, logits, q = two_stage(LOCAL, W, A, B, h, token_ids, T, k_tile)
+
+Offline preparation of A and B (the Freq-aware SVD) is in
+draft_lm_head_gb300.prep.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from ._lib import LIB_PATH, LmheadError, check, load, status_string  # noqa: F401
+
+GLOBAL = 0
+LOCAL = 1
+
+__all__ = [
+    "GLOBAL", "LOCAL", "LmheadError", "candidate_count", "workspace_size", "project_u",
+    "lowrank_score_topk", "gather_logits", "candidate_softmax", "two_stage", "dense_head",
+    "pruned_head", "last_device_error", "version", "Workspace",
+]
+
+_BF16_OK = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (
+    torch.bfloat16, torch.int16)
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _bf16(t: torch.Tensor, name: str) -> int:
+    if not t.is_cuda or t.dtype not in _BF16_OK or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous CUDA bf16 tensor, got {t.dtype} "
+                        f"on {t.device} (contiguous={t.is_contiguous()})")
+    return t.data_ptr()
+
+
+def _typed(t: Optional[torch.Tensor], dtype, name: str) -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous CUDA {dtype} tensor")
+    return t.data_ptr()
+
+
+def version() -> int:
+    return load().lmhead_version()
+
+
+def candidate_count(mode: int, n: int, C_or_tile: int, k_tile: int = 0) -> int:
+    K = load().lmhead_candidate_count(mode, n, C_or_tile, k_tile)
+    if K < 0:
+        raise LmheadError(int(K), "candidate_count")
+    return int(K)
+
+
+def workspace_size(mode: int, n: int, d: int, r: int, M: int, C_or_tile: int,
+                   k_tile: int = 0) -> int:
+    return int(load().lmhead_workspace_size(mode, n, d, r, M, C_or_tile, k_tile))
+
+
+class Workspace:
+    """A reusable device workspace (grows on demand; 256-byte aligned)."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int, device) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != device:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        return self.buf
+
+
+def _ws(workspace, nbytes, device):
+    if workspace is None:
+        return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    if isinstance(workspace, Workspace):
+        return workspace.get(nbytes, device)
+    return workspace
+
+
+def project_u(B: torch.Tensor, h: torch.Tensor, out: Optional[torch.Tensor] = None,
+              stream=None) -> torch.Tensor:
+    r, d = B.shape
+    M = h.shape[0]
+    u = out if out is not None else torch.empty((M, r), dtype=torch.bfloat16, device=h.device)
+    check(load().lmhead_project_u(_bf16(B, "B"), _bf16(h, "h"), d, r, M, _bf16(u, "u"),
+                                  _stream_ptr(stream)), "project_u")
+    return u
+
+
+def lowrank_score_topk(mode: int, A: torch.Tensor, B: torch.Tensor, h: torch.Tensor,
+                       token_ids: Optional[torch.Tensor], C_or_tile: int, k_tile: int = 0,
+                       with_scores: bool = False, workspace=None, stream=None):
+    n, r = A.shape
+    d = B.shape[1]
+    M = h.shape[0]
+    K = candidate_count(mode, n, C_or_tile, k_tile)
+    ids = torch.empty((M, K), dtype=torch.int32, device=h.device)
+    scores = torch.empty((M, K), dtype=torch.float32, device=h.device) if with_scores else None
+    nbytes = workspace_size(mode, n, d, r, M, C_or_tile, k_tile)
+    ws = _ws(workspace, nbytes, h.device)
+    check(load().lmhead_lowrank_score_topk(
+        mode, _bf16(A, "A"), _bf16(B, "B"), _bf16(h, "h"), _typed(token_ids, torch.int32, "token_ids"),
+        n, d, r, M, C_or_tile, k_tile, ids.data_ptr(), _typed(scores, torch.float32, "scores"),
+        ws.data_ptr(), ws.numel(), _stream_ptr(stream)), "lowrank_score_topk")
+    return (ids, scores) if with_scores else ids
+
+
+def gather_logits(W: torch.Tensor, h: torch.Tensor, ids: torch.Tensor,
+                  out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    n, d = W.shape
+    M, K = ids.shape
+    L = out if out is not None else torch.empty((M, K), dtype=torch.float32, device=h.device)
+    check(load().lmhead_gather_logits(_bf16(W, "W"), _bf16(h, "h"), _typed(ids, torch.int32, "ids"),
+                                      n, d, M, K, _typed(L, torch.float32, "out"),
+                                      _stream_ptr(stream)), "gather_logits")
+    return L
+
+
+def candidate_softmax(logits: torch.Tensor, temperature: float = 1.0,
+                      out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    M, K = logits.shape
+    q = out if out is not None else torch.empty_like(logits)
+    check(load().lmhead_candidate_softmax(_typed(logits, torch.float32, "logits"), M, K,
+                                          float(temperature), _typed(q, torch.float32, "out"),
+                                          _stream_ptr(stream)), "candidate_softmax")
+    return q
+
+
+def two_stage(mode: int, W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, h: torch.Tensor,
+              token_ids: Optional[torch.Tensor], C_or_tile: int, k_tile: int = 0,
+              temperature: float = 1.0, workspace=None, out=None, stream=None):
+    """The whole head: returns (ids, logits, q), each M x K."""
+    n, d = W.shape
+    r = A.shape[1]
+    M = h.shape[0]
+    K = candidate_count(mode, n, C_or_tile, k_tile)
+    if out is None:
+        ids = torch.empty((M, K), dtype=torch.int32, device=h.device)
+        L = torch.empty((M, K), dtype=torch.float32, device=h.device)
+        q = torch.empty((M, K), dtype=torch.float32, device=h.device)
+    else:
+        ids, L, q = out
+    nbytes = workspace_size(mode, n, d, r, M, C_or_tile, k_tile)
+    ws = _ws(workspace, nbytes, h.device)
+    check(load().lmhead_two_stage(
+        mode, _bf16(W, "W"), _bf16(A, "A"), _bf16(B, "B"), _bf16(h, "h"),
+        _typed(token_ids, torch.int32, "token_ids"), n, d, r, M, C_or_tile, k_tile,
+        float(temperature), _typed(ids, torch.int32, "ids"), _typed(L, torch.float32, "logits"),
+        _typed(q, torch.float32, "q"), ws.data_ptr(), ws.numel(), _stream_ptr(stream)),
+        "two_stage")
+    return ids, L, q
+
+
+def dense_head(W: torch.Tensor, h: torch.Tensor, temperature: float = 1.0, with_q: bool = True,
+               out=None, stream=None):
+    n, d = W.shape
+    M = h.shape[0]
+    if out is None:
+        L = torch.empty((M, n), dtype=torch.float32, device=h.device)
+        q = torch.empty((M, n), dtype=torch.float32, device=h.device) if with_q else None
+    else:
+        L, q = out
+    check(load().lmhead_dense_head(_bf16(W, "W"), _bf16(h, "h"), n, d, M, float(temperature),
+                                   _typed(L, torch.float32, "logits"), _typed(q, torch.float32, "q"),
+                                   _stream_ptr(stream)), "dense_head")
+    return L, q
+
+
+def pruned_head(W_pruned: torch.Tensor, h: torch.Tensor, temperature: float = 1.0,
+                with_q: bool = True, out=None, stream=None):
+    n_keep, d = W_pruned.shape
+    M = h.shape[0]
+    if out is None:
+        L = torch.empty((M, n_keep), dtype=torch.float32, device=h.device)
+        q = torch.empty((M, n_keep), dtype=torch.float32, device=h.device) if with_q else None
+    else:
+        L, q = out
+    check(load().lmhead_pruned_head(_bf16(W_pruned, "W_pruned"), _bf16(h, "h"), n_keep, d, M,
+                                    float(temperature), _typed(L, torch.float32, "logits"),
+                                    _typed(q, torch.float32, "q"), _stream_ptr(stream)),
+          "pruned_head")
+    return L, q
+
+
+def last_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load().lmhead_last_device_error(_stream_ptr(stream)))

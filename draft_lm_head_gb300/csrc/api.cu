@@ -1,0 +1,258 @@
+// The C ABI of liblmhead (include/lmhead.h): host-side validation, workspace
+// carve-up and the launch sequence of each entry point. No entry point
+// allocates device memory or synchronises (except lmhead_last_device_error).
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "lmhead.h"
+
+namespace lmhead {
+
+__device__ int g_device_error;
+
+int* device_error_word() {
+  static int* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+namespace {
+
+constexpr int kMaxR = 2048;
+constexpr int kMaxD = 65536;
+constexpr int kMaxM = 65535 * 8;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+  size_t u = 0, tickets = 0, scores = 0, total = 0;
+};
+
+bool needs_score_buffer(int mode, int k_tile) {
+  return mode == LMHEAD_GLOBAL || k_tile > kFusedMaxKTile;
+}
+
+Layout layout_for(int mode, int64_t n, int r, int M, int k_tile) {
+  Layout L;
+  size_t off = 0;
+  L.u = off;
+  off = round_up(off + (size_t)M * r * sizeof(bf16_t), 256);
+  L.tickets = off;
+  off = round_up(off + (size_t)M * sizeof(int), 256);
+  if (needs_score_buffer(mode, k_tile)) {
+    L.scores = off;
+    off = round_up(off + (size_t)M * (size_t)n * sizeof(float), 256);
+  }
+  L.total = off;
+  return L;
+}
+
+int64_t candidate_count(int mode, int64_t n, int C_or_tile, int k_tile) {
+  if (n < 1 || n > INT32_MAX) return LMHEAD_ERR_SHAPE;
+  if (mode == LMHEAD_GLOBAL) {
+    if (C_or_tile < 1 || C_or_tile > n) return LMHEAD_ERR_SHAPE;
+    return C_or_tile;
+  }
+  if (mode == LMHEAD_LOCAL) {
+    if (C_or_tile < 1 || k_tile < 1 || k_tile > C_or_tile) return LMHEAD_ERR_SHAPE;
+    const int64_t T = C_or_tile;
+    const int64_t full = n / T, tail = n - full * T;
+    return full * k_tile + (tail ? (tail < k_tile ? tail : k_tile) : 0);
+  }
+  return LMHEAD_ERR_SHAPE;
+}
+
+int check_select(int mode, int64_t n, int d, int r, int M, int C_or_tile, int k_tile) {
+  if (d < 8 || d % 8 || d > kMaxD || r < 8 || r % 8 || r > kMaxR) return LMHEAD_ERR_SHAPE;
+  if (M < 1 || M > kMaxM) return LMHEAD_ERR_SHAPE;
+  const int64_t K = candidate_count(mode, n, C_or_tile, k_tile);
+  if (K < 0) return (int)K;
+  if (mode == LMHEAD_GLOBAL && C_or_tile > kSelectMaxK) return LMHEAD_ERR_UNSUPPORTED;
+  if (mode == LMHEAD_LOCAL && k_tile > kSelectMaxK) return LMHEAD_ERR_UNSUPPORTED;
+  if ((int64_t)M * K > INT32_MAX) return LMHEAD_ERR_SHAPE;
+  return LMHEAD_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? LMHEAD_OK : LMHEAD_ERR_CUDA; }
+
+// Stage 1 on validated arguments; u lives in the workspace.
+int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
+               const int32_t* token_ids, int64_t n, int d, int r, int M, int C_or_tile,
+               int k_tile, int32_t* out_ids, float* out_scores, char* ws, const Layout& L,
+               bool zero_tickets, cudaStream_t s) {
+  bf16_t* u = reinterpret_cast<bf16_t*>(ws + L.u);
+  int* tickets = reinterpret_cast<int*>(ws + L.tickets);
+  cudaError_t e = launch_project_u(B, h, d, r, M, u, zero_tickets ? tickets : nullptr, M, s);
+  if (e != cudaSuccess) return LMHEAD_ERR_CUDA;
+  if (!needs_score_buffer(mode, k_tile)) {
+    e = launch_local_topk_fma(A, u, token_ids, n, r, M, C_or_tile, k_tile, out_ids, out_scores, s);
+    return cuda_status(e);
+  }
+  float* S = reinterpret_cast<float*>(ws + L.scores);
+  e = launch_score_all_fma(A, u, n, r, M, S, s);
+  if (e != cudaSuccess) return LMHEAD_ERR_CUDA;
+  const int64_t seg = mode == LMHEAD_GLOBAL ? n : C_or_tile;
+  const int k = mode == LMHEAD_GLOBAL ? C_or_tile : k_tile;
+  e = launch_segment_topk(S, token_ids, n, M, seg, k, out_ids, out_scores, device_error_word(), s);
+  return cuda_status(e);
+}
+
+bool valid_temperature(float t) { return t > 0.f && isfinite(t); }
+
+}  // namespace
+}  // namespace lmhead
+
+using namespace lmhead;
+
+extern "C" {
+
+int lmhead_version(void) { return 100; }
+
+const char* lmhead_status_string(int status) {
+  switch (status) {
+    case LMHEAD_OK: return "ok";
+    case LMHEAD_ERR_NULL: return "null pointer argument";
+    case LMHEAD_ERR_SHAPE: return "invalid size argument";
+    case LMHEAD_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case LMHEAD_ERR_WORKSPACE: return "workspace missing or too small";
+    case LMHEAD_ERR_UNSUPPORTED: return "unsupported configuration";
+    case LMHEAD_ERR_CUDA: return "CUDA error";
+    case LMHEAD_ERR_DEVICE_CHECK: return "device-side check failed (e.g. id out of range)";
+    case LMHEAD_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int64_t lmhead_candidate_count(int mode, int64_t n, int C_or_tile, int k_tile) {
+  return candidate_count(mode, n, C_or_tile, k_tile);
+}
+
+size_t lmhead_workspace_size(int mode, int64_t n, int d, int r, int M, int C_or_tile,
+                             int k_tile) {
+  if (check_select(mode, n, d, r, M, C_or_tile, k_tile) != LMHEAD_OK) return 0;
+  return layout_for(mode, n, r, M, k_tile).total;
+}
+
+int lmhead_project_u(const lmhead_bf16* B, const lmhead_bf16* h, int d, int r, int M,
+                     lmhead_bf16* u, lmhead_stream stream) {
+  if (!B || !h || !u) return LMHEAD_ERR_NULL;
+  if (d < 8 || d % 8 || d > kMaxD || r < 1 || r > 65535 * 8 || M < 1 || M > kMaxM)
+    return LMHEAD_ERR_SHAPE;
+  if (!aligned16(B) || !aligned16(h)) return LMHEAD_ERR_ALIGN;
+  return cuda_status(launch_project_u(B, h, d, r, M, u, nullptr, 0, (cudaStream_t)stream));
+}
+
+int lmhead_lowrank_score_topk(int mode, const lmhead_bf16* A, const lmhead_bf16* B,
+                              const lmhead_bf16* h, const int32_t* token_ids, int64_t n, int d,
+                              int r, int M, int C_or_tile, int k_tile, int32_t* out_ids,
+                              float* out_scores, void* workspace, size_t workspace_bytes,
+                              lmhead_stream stream) {
+  if (!A || !B || !h || !out_ids) return LMHEAD_ERR_NULL;
+  if (mode == LMHEAD_GLOBAL) k_tile = 0;
+  int st = check_select(mode, n, d, r, M, C_or_tile, k_tile);
+  if (st != LMHEAD_OK) return st;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(h) || (token_ids && !aligned16(token_ids)) ||
+      !aligned16(out_ids) || (out_scores && !aligned16(out_scores)))
+    return LMHEAD_ERR_ALIGN;
+  const Layout L = layout_for(mode, n, r, M, k_tile);
+  if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return LMHEAD_ERR_WORKSPACE;
+  return run_select(mode, A, B, h, token_ids, n, d, r, M, C_or_tile, k_tile, out_ids, out_scores,
+                    static_cast<char*>(workspace), L, false, (cudaStream_t)stream);
+}
+
+int lmhead_gather_logits(const lmhead_bf16* W, const lmhead_bf16* h, const int32_t* ids,
+                         int64_t n, int d, int M, int K, float* out_logits,
+                         lmhead_stream stream) {
+  if (!W || !h || !ids || !out_logits) return LMHEAD_ERR_NULL;
+  if (n < 1 || n > INT32_MAX || d < 8 || d % 8 || d > kMaxD || M < 1 || K < 1 ||
+      (int64_t)M * K > INT32_MAX)
+    return LMHEAD_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(h)) return LMHEAD_ERR_ALIGN;
+  return cuda_status(launch_gather_logits(W, h, ids, n, d, M, K, out_logits, nullptr, 1.f,
+                                          nullptr, device_error_word(), (cudaStream_t)stream));
+}
+
+int lmhead_candidate_softmax(const float* logits, int M, int K, float temperature, float* out_q,
+                             lmhead_stream stream) {
+  if (!logits || !out_q) return LMHEAD_ERR_NULL;
+  if (M < 1 || K < 1 || M > 2147483647 / K) return LMHEAD_ERR_SHAPE;
+  if (!valid_temperature(temperature)) return LMHEAD_ERR_SHAPE;
+  return cuda_status(launch_row_softmax(logits, M, K, 1.f / temperature, out_q,
+                                        (cudaStream_t)stream));
+}
+
+int lmhead_two_stage(int mode, const lmhead_bf16* W, const lmhead_bf16* A, const lmhead_bf16* B,
+                     const lmhead_bf16* h, const int32_t* token_ids, int64_t n, int d, int r,
+                     int M, int C_or_tile, int k_tile, float temperature, int32_t* out_ids,
+                     float* out_logits, float* out_q, void* workspace, size_t workspace_bytes,
+                     lmhead_stream stream) {
+  if (!W || !A || !B || !h || !out_ids || !out_logits || !out_q) return LMHEAD_ERR_NULL;
+  if (mode == LMHEAD_GLOBAL) k_tile = 0;
+  int st = check_select(mode, n, d, r, M, C_or_tile, k_tile);
+  if (st != LMHEAD_OK) return st;
+  if (!valid_temperature(temperature)) return LMHEAD_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(A) || !aligned16(B) || !aligned16(h) ||
+      (token_ids && !aligned16(token_ids)) || !aligned16(out_ids))
+    return LMHEAD_ERR_ALIGN;
+  const Layout L = layout_for(mode, n, r, M, k_tile);
+  if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return LMHEAD_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+  st = run_select(mode, A, B, h, token_ids, n, d, r, M, C_or_tile, k_tile, out_ids, nullptr, ws,
+                  L, true, s);
+  if (st != LMHEAD_OK) return st;
+  const int K = (int)candidate_count(mode, n, C_or_tile, k_tile);
+  return cuda_status(launch_gather_logits(W, h, out_ids, n, d, M, K, out_logits, out_q,
+                                          1.f / temperature,
+                                          reinterpret_cast<int*>(ws + L.tickets),
+                                          device_error_word(), s));
+}
+
+int lmhead_dense_head(const lmhead_bf16* W, const lmhead_bf16* h, int64_t n, int d, int M,
+                      float temperature, float* out_logits, float* out_q, lmhead_stream stream) {
+  if (!W || !h || !out_logits) return LMHEAD_ERR_NULL;
+  if (n < 1 || n > INT32_MAX || d < 8 || d % 8 || d > kMaxD || M < 1 || M > 65535)
+    return LMHEAD_ERR_SHAPE;
+  if (out_q && !valid_temperature(temperature)) return LMHEAD_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(h)) return LMHEAD_ERR_ALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_dense_logits(W, h, n, d, M, out_logits, s);
+  if (e != cudaSuccess || !out_q) return cuda_status(e);
+  return cuda_status(launch_row_softmax(out_logits, M, n, 1.f / temperature, out_q, s));
+}
+
+int lmhead_pruned_head(const lmhead_bf16* W_pruned, const lmhead_bf16* h, int n_keep, int d,
+                       int M, float temperature, float* out_logits, float* out_q,
+                       lmhead_stream stream) {
+  return lmhead_dense_head(W_pruned, h, n_keep, d, M, temperature, out_logits, out_q, stream);
+}
+
+int lmhead_last_device_error(lmhead_stream stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LMHEAD_ERR_CUDA;
+  int* p = device_error_word();
+  if (!p) return LMHEAD_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return LMHEAD_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return LMHEAD_ERR_CUDA;
+  }
+  if (v == kDevErrBadId) return LMHEAD_ERR_DEVICE_CHECK;
+  if (v == kDevErrTimeout) return LMHEAD_ERR_TIMEOUT;
+  return v == 0 ? LMHEAD_OK : LMHEAD_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Shared device helpers of liblmhead (bf16 unpacking, order-preserving keys,
+// warp reductions, the device error word).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lmhead.h"
+
+namespace lmhead {
+
+constexpr int kWarp = 32;
+
+// Error word values (a kernel never traps: it records and carries on).
+constexpr int kDevErrBadId = 1;
+constexpr int kDevErrTimeout = 2;
+
+__device__ __forceinline__ void record_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// 8 bf16 packed in a uint4 -> 8 floats (bf16 -> fp32 is exact: shift left 16).
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
+  float fa[8], fb[8];
+  unpack8(a, fa);
+  unpack8(b, fb);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s = fmaf(fa[i], fb[i], s);
+  return s;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// fp32 -> uint32 whose unsigned order is the float order (-0 folded into +0).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_float(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
+// Unique 64-bit selection key: score order first, then the smaller
+// vocabulary id wins among equal scores.
+__device__ __forceinline__ uint64_t select_key(float score, int32_t vocab_id) {
+  return (static_cast<uint64_t>(float_key(score)) << 32) |
+         static_cast<uint32_t>(~static_cast<uint32_t>(vocab_id));
+}
+
+__device__ __forceinline__ int32_t key_id(uint64_t k) {
+  return static_cast<int32_t>(~static_cast<uint32_t>(k & 0xFFFFFFFFull));
+}
+
+__device__ __forceinline__ float key_score(uint64_t k) {
+  return key_float(static_cast<uint32_t>(k >> 32));
+}
+
+// (score desc, id asc) "a beats b".
+__device__ __forceinline__ bool beats(float sa, int32_t ia, float sb, int32_t ib) {
+  return sa > sb || (sa == sb && ia < ib);
+}
+
+}  // namespace lmhead

@@ -1,0 +1,53 @@
+// Internal launch functions of liblmhead (host side). Each returns a
+// cudaError_t from the launch; arguments have been validated by api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lmhead {
+
+typedef uint16_t bf16_t;
+
+// Largest k_tile handled by the fused score + tile top-k kernels.
+constexpr int kFusedMaxKTile = 32;
+// Largest selection budget of the radix select (global C or k_tile).
+constexpr int kSelectMaxK = 4096;
+
+// K1: u = bf16(B h), fp32 accumulation. Also zeroes `zero_ints` ints at
+// `zero_ptr` (per-row tickets of the fused softmax), if non-null.
+cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int M, bf16_t* u,
+                             int* zero_ptr, int zero_ints, cudaStream_t s);
+
+// K4 (CUDA cores): fused tile scores + per-tile top-k_tile, no score writeback.
+cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
+                                  int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,
+                                  float* out_scores, cudaStream_t s);
+
+// K2 (CUDA cores): S[m, p] = A[p] . u[m] for every position p, fp32 to HBM.
+cudaError_t launch_score_all_fma(const bf16_t* A, const bf16_t* u, int64_t n, int r, int M,
+                                 float* S, cudaStream_t s);
+
+// K3: per row m, per segment of `seg_len` positions, exact top-k of S by
+// (score desc, vocabulary id asc). k <= kSelectMaxK.
+cudaError_t launch_segment_topk(const float* S, const int32_t* token_ids, int64_t n, int M,
+                                int64_t seg_len, int k, int32_t* out_ids, float* out_scores,
+                                int* err, cudaStream_t s);
+
+// K5 (+K6 fused when q != nullptr): L[m,j] = W[ids[m,j]] . h[m]; q = softmax.
+// `tickets` (M ints, zero on entry, left zero on exit) enable the fusion.
+cudaError_t launch_gather_logits(const bf16_t* W, const bf16_t* h, const int32_t* ids, int64_t n,
+                                 int d, int M, int K, float* logits, float* q, float inv_temp,
+                                 int* tickets, int* err, cudaStream_t s);
+
+// K6 standalone: row softmax of an M x K matrix (any K).
+cudaError_t launch_row_softmax(const float* L, int M, int64_t K, float inv_temp, float* q,
+                               cudaStream_t s);
+
+// K7: dense logits over all rows of W (n x d).
+cudaError_t launch_dense_logits(const bf16_t* W, const bf16_t* h, int64_t n, int d, int M,
+                                float* logits, cudaStream_t s);
+
+int* device_error_word();  // this device's error word (nullptr on failure)
+
+}  // namespace lmhead

@@ -1,0 +1,187 @@
+// K3: exact Top-k over segments of a score matrix (EAGLE-4 notes, "A Local
+// Top-k based variant": the original flow's ids = topk(scores, C) reads the
+// full-vocabulary scores back from HBM).
+//
+// A segment is `seg_len` consecutive positions of one row of S (M x n fp32);
+// the global Top-C is one segment of length n, the local variant with a large
+// k_tile is one segment per tile. Order: score descending, then the smaller
+// vocabulary id (token_ids[p], identity when null). Every element maps to a
+// unique 64-bit key (order-preserving score bits, then the complemented id),
+// so the k-th largest key is a unique threshold.
+//
+// Long segments: multi-pass radix select on 12-bit digits of the key (each
+// pass one read of the segment, histogram in shared memory) until the
+// boundary digit holds few enough keys for shared memory, then one collection
+// pass and a bitonic sort of the survivors. Short segments (<= 8192 keys):
+// loaded whole and bitonic-sorted.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lmhead {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kCap = kSelectMaxK;  // keys of the selected / candidate regions
+constexpr int kBins = 4096;        // 12-bit digits
+constexpr int kDigit = 12;
+
+__device__ __forceinline__ uint64_t key_at(const float* __restrict__ row,
+                                           const int32_t* __restrict__ token_ids, int64_t p) {
+  const int32_t id = token_ids ? __ldg(token_ids + p) : (int32_t)p;
+  return select_key(__ldcg(row + p), id);
+}
+
+// Sort keys[0..P) descending, P a power of two, all threads participate.
+__device__ void bitonic_desc(uint64_t* keys, int P) {
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (P >> 1); i += blockDim.x) {
+        const int pos = 2 * i - (i & (stride - 1));
+        const int par = pos + stride;
+        const uint64_t a = keys[pos], b = keys[par];
+        const bool desc_block = (pos & size) == 0;
+        if (desc_block ? (a < b) : (a > b)) {
+          keys[pos] = b;
+          keys[par] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__device__ __forceinline__ int pow2_at_least(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// grid: (segments, M). Dynamic smem: 2*kCap keys + kBins counters + scan.
+__global__ void __launch_bounds__(kThreads)
+segment_topk_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_ids,
+                    int64_t n, int64_t seg_len, int k, int K, int32_t* __restrict__ out_ids,
+                    float* __restrict__ out_scores) {
+  extern __shared__ uint64_t keys[];  // [0,kCap) selected, [kCap,2kCap) candidates
+  uint32_t* hist = reinterpret_cast<uint32_t*>(keys + 2 * kCap);
+  uint32_t* part = hist + kBins;  // kThreads partial sums
+  __shared__ uint64_t s_lo, s_hi;
+  __shared__ int s_gt, s_bin_count, s_sel, s_cand;
+
+  const int tid = threadIdx.x;
+  const int m = blockIdx.y;
+  const int64_t seg = blockIdx.x;
+  const int64_t p0 = seg * seg_len;
+  const int64_t p1 = min(n, p0 + seg_len);
+  const int len = (int)(p1 - p0);
+  const int kk = min(k, len);
+  const float* row = S + (size_t)m * n;
+  const size_t obase = (size_t)m * K + (size_t)seg * k;
+
+  if (len <= 2 * kCap) {
+    const int P = pow2_at_least(len);
+    for (int i = tid; i < P; i += blockDim.x) keys[i] = i < len ? key_at(row, token_ids, p0 + i) : 0ull;
+    __syncthreads();
+    bitonic_desc(keys, P);
+    for (int j = tid; j < kk; j += blockDim.x) {
+      out_ids[obase + j] = key_id(keys[j]);
+      if (out_scores) out_scores[obase + j] = key_score(keys[j]);
+    }
+    return;
+  }
+
+  uint64_t lo = 0ull, hi = ~0ull;
+  int gt = 0;  // keys above hi (all selected)
+  for (int shift = 64 - kDigit;; shift = shift >= kDigit ? shift - kDigit : 0) {
+    for (int i = tid; i < kBins; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int64_t p = p0 + tid; p < p1; p += blockDim.x) {
+      const uint64_t key = key_at(row, token_ids, p);
+      if (key >= lo && key <= hi) atomicAdd(&hist[(key >> shift) & (kBins - 1)], 1u);
+    }
+    __syncthreads();
+    // suffix sums over threads' groups of 4 bins (bins descending = keys descending)
+    const int g = kThreads - 1 - tid;  // thread tid owns bins [4g, 4g+4)
+    uint32_t local = hist[4 * g] + hist[4 * g + 1] + hist[4 * g + 2] + hist[4 * g + 3];
+    part[tid] = local;
+    __syncthreads();
+    for (int off = 1; off < kThreads; off <<= 1) {
+      const uint32_t v = tid >= off ? part[tid - off] : 0u;
+      __syncthreads();
+      part[tid] += v;
+      __syncthreads();
+    }
+    // part[tid] = keys in bins >= 4g (inclusive); above = keys in bins >= 4g+4
+    uint32_t above = part[tid] - local;
+    const uint32_t need = (uint32_t)(kk - gt);
+    if (above < need && above + local >= need) {
+      for (int b = 4 * g + 3; b >= 4 * g; --b) {
+        if (above + hist[b] >= need) {
+          s_gt = gt + (int)above;
+          s_bin_count = (int)hist[b];
+          const uint64_t prefix = (lo & ~((((uint64_t)kBins - 1) << shift) | ((1ull << shift) - 1ull)));
+          const uint64_t nlo = prefix | ((uint64_t)b << shift);
+          s_lo = nlo;
+          s_hi = nlo | ((1ull << shift) - 1ull);
+          break;
+        }
+        above += hist[b];
+      }
+    }
+    __syncthreads();
+    lo = s_lo;
+    hi = s_hi;
+    gt = s_gt;
+    const int bin_count = s_bin_count;
+    __syncthreads();
+    if (bin_count <= kCap || shift == 0) break;
+  }
+
+  if (tid == 0) { s_sel = 0; s_cand = 0; }
+  __syncthreads();
+  for (int64_t p = p0 + tid; p < p1; p += blockDim.x) {
+    const uint64_t key = key_at(row, token_ids, p);
+    if (key > hi) {
+      keys[atomicAdd(&s_sel, 1)] = key;
+    } else if (key >= lo) {
+      const int c = atomicAdd(&s_cand, 1);
+      if (c < kCap) keys[kCap + c] = key;
+    }
+  }
+  __syncthreads();
+  const int ncand = min(s_cand, kCap);
+  const int P = pow2_at_least(ncand);
+  for (int i = ncand + tid; i < P; i += blockDim.x) keys[kCap + i] = 0ull;
+  __syncthreads();
+  bitonic_desc(keys + kCap, P);
+  const int take = kk - gt;
+  for (int i = tid; i < take; i += blockDim.x) keys[gt + i] = keys[kCap + i];
+  const int Ps = pow2_at_least(kk);
+  for (int i = kk + tid; i < Ps; i += blockDim.x) keys[i] = 0ull;
+  __syncthreads();
+  bitonic_desc(keys, Ps);
+  for (int j = tid; j < kk; j += blockDim.x) {
+    out_ids[obase + j] = key_id(keys[j]);
+    if (out_scores) out_scores[obase + j] = key_score(keys[j]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_segment_topk(const float* S, const int32_t* token_ids, int64_t n, int M,
+                                int64_t seg_len, int k, int32_t* out_ids, float* out_scores,
+                                int* err, cudaStream_t s) {
+  (void)err;
+  const int64_t segs = (n + seg_len - 1) / seg_len;
+  const int64_t full = n / seg_len, tail = n - full * seg_len;
+  const int K = (int)(full * k + (tail ? (tail < k ? tail : k) : 0));
+  const size_t smem = 2 * kCap * sizeof(uint64_t) + (kBins + kThreads) * sizeof(uint32_t);
+  cudaError_t e = cudaFuncSetAttribute(segment_topk_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)segs, M);
+  segment_topk_kernel<<<grid, kThreads, smem, s>>>(S, token_ids, n, seg_len, k, K, out_ids,
+                                                   out_scores);
+  return cudaGetLastError();
+}
+
+}  // namespace lmhead

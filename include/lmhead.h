@@ -1,0 +1,195 @@
+/*
+ * lmhead.h - C ABI of liblmhead.so, a GB300 (sm_103a) two-stage draft LM head.
+ *
+ * The operation is the "EAGLE Efficient LM Head" of the EAGLE-4 design notes
+ * (qingkeai.online/blog/EAGLE): stage 1 scores the whole vocabulary with a
+ * rank-r factor of the full head, A (n x r) and B (r x d), built offline by
+ * the Freq-aware SVD of that page's section "A training-free version:
+ * Freq-aware SVD", and keeps candidates by Top-k (globally, or per vocabulary
+ * tile as in the section "A Local Top-k based variant"); stage 2 gathers the
+ * candidates' rows of the full head W (n x d), recomputes their exact logits
+ * from the same hidden states h (M x d) and softmaxes them into the draft
+ * distribution q that a speculative-decoding drafter samples from.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Element types: bf16 tensors are passed as raw 16-bit patterns
+ *    (lmhead_bf16); scores, logits and q are fp32; ids are int32 vocabulary
+ *    ids. All matrices are dense row-major with no padding.
+ *  - Memory: every pointer is a DEVICE pointer owned by the caller, aligned
+ *    to 16 bytes; d and r must be multiples of 8. The library allocates no
+ *    device memory; scratch comes from the caller's `workspace`
+ *    (size from lmhead_workspace_size). `workspace` may be reused across
+ *    calls but not by two calls in flight at once.
+ *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream). All
+ *    calls enqueue asynchronous work on it and return without synchronising,
+ *    except lmhead_last_device_error.
+ *  - Errors: arguments are validated on the host before anything is
+ *    launched; a negative lmhead_status is returned and nothing is enqueued.
+ *    A failed launch returns LMHEAD_ERR_CUDA. Kernels that read caller ids
+ *    bounds-check them; a bad id sets a device error word (read with
+ *    lmhead_last_device_error) and its outputs are NaN; nothing faults.
+ *    NaN/Inf inputs are not checked (outputs undefined).
+ *  - Ties: equal scores are ordered by the smaller vocabulary id.
+ */
+#ifndef LMHEAD_H
+#define LMHEAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t lmhead_bf16; /* bf16 bit pattern */
+typedef void* lmhead_stream; /* a cudaStream_t */
+
+typedef enum {
+  LMHEAD_OK = 0,
+  LMHEAD_ERR_NULL = -1,         /* a required pointer is NULL */
+  LMHEAD_ERR_SHAPE = -2,        /* a size is out of range or inconsistent */
+  LMHEAD_ERR_ALIGN = -3,        /* a pointer is not 16-byte aligned */
+  LMHEAD_ERR_WORKSPACE = -4,    /* workspace missing or too small */
+  LMHEAD_ERR_UNSUPPORTED = -5,  /* valid but not supported by this build */
+  LMHEAD_ERR_CUDA = -6,         /* a CUDA runtime call or launch failed */
+  LMHEAD_ERR_DEVICE_CHECK = -7, /* a kernel's own check failed (bad id, ...) */
+  LMHEAD_ERR_TIMEOUT = -8       /* a kernel's bounded wait ran out */
+} lmhead_status;
+
+typedef enum {
+  LMHEAD_GLOBAL = 0, /* ids = Top-C of the full-vocabulary scores */
+  LMHEAD_LOCAL = 1   /* ids = concat over vocabulary tiles of each tile's top-k_tile */
+} lmhead_mode;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int lmhead_version(void);
+
+/* Human-readable name of a status code; never NULL. */
+const char* lmhead_status_string(int status);
+
+/*
+ * Candidates per hidden vector for a mode (EAGLE-4 notes, "A Local Top-k
+ * based variant": the candidate count is about tiles x k_tile).
+ *   GLOBAL: C (C_or_tile), requires 1 <= C <= n.
+ *   LOCAL : T = C_or_tile rows per tile, tiles = ceil(n/T); each full tile
+ *           keeps k_tile and a short last tile keeps min(k_tile, rows).
+ * Returns the count, or a negative lmhead_status for invalid sizes.
+ */
+int64_t lmhead_candidate_count(int mode, int64_t n, int C_or_tile, int k_tile);
+
+/*
+ * Bytes of device workspace that lmhead_lowrank_score_topk and
+ * lmhead_two_stage need for these sizes. Depends only on its arguments.
+ * Returns 0 for invalid sizes.
+ */
+size_t lmhead_workspace_size(int mode, int64_t n, int d, int r, int M,
+                             int C_or_tile, int k_tile);
+
+/*
+ * Stage-1 projection u = B.h (EAGLE-4 notes, "A Local Top-k based variant",
+ * first line of both flows).
+ *   B  r x d bf16, h  M x d bf16  ->  u  M x r bf16.
+ * Accumulates in fp32 and rounds each u element to bf16 (nearest-even).
+ */
+int lmhead_project_u(const lmhead_bf16* B, const lmhead_bf16* h, int d, int r, int M,
+                     lmhead_bf16* u, lmhead_stream stream);
+
+/*
+ * Stage 1: candidate selection with the low-rank head (EAGLE-4 notes,
+ * "A training-free version: Freq-aware SVD": Top-k of A(Bh); and
+ * "A Local Top-k based variant").
+ *   A          n x r bf16, rows in POSITION order (pre-shuffled: position p
+ *              holds vocabulary row token_ids[p]).
+ *   B          r x d bf16.
+ *   h          M x d bf16 hidden states; each row is selected independently.
+ *   token_ids  n int32, position -> vocabulary id; NULL means identity.
+ *              Must be a permutation of 0..n-1 (ids are range-checked).
+ *   mode       LMHEAD_GLOBAL: C_or_tile = C, k_tile ignored (0).
+ *              LMHEAD_LOCAL : C_or_tile = T >= 1, 1 <= k_tile <= T.
+ *   out_ids    M x K int32 (K = lmhead_candidate_count). GLOBAL rows are in
+ *              descending score order; LOCAL rows are in tile order, each
+ *              tile's ids in descending score order.
+ *   out_scores M x K fp32 low-rank scores of out_ids, or NULL.
+ *   workspace  >= lmhead_workspace_size(...) bytes, 256-byte aligned.
+ * LOCAL mode with k_tile <= 32 runs the fused score + tile top-k kernel
+ * (no score writeback); GLOBAL mode and larger k_tile write the fp32 scores
+ * to the workspace and run a radix select.
+ */
+int lmhead_lowrank_score_topk(int mode, const lmhead_bf16* A, const lmhead_bf16* B,
+                              const lmhead_bf16* h, const int32_t* token_ids,
+                              int64_t n, int d, int r, int M, int C_or_tile, int k_tile,
+                              int32_t* out_ids, float* out_scores,
+                              void* workspace, size_t workspace_bytes,
+                              lmhead_stream stream);
+
+/*
+ * Stage 2: exact logits of the candidates (EAGLE-4 notes, "EAGLE Efficient
+ * LM Head": index the full head's rows of the candidates and recompute the
+ * logits with the original hidden states; logits = W[ids] @ h).
+ *   W  n x d bf16 (vocabulary order), h  M x d bf16, ids  M x K int32.
+ *   out_logits M x K fp32: out_logits[m,j] = sum_i W[ids[m,j], i] * h[m,i],
+ *   fp32 accumulation. An id outside [0, n) gives NaN and sets the device
+ *   error word.
+ */
+int lmhead_gather_logits(const lmhead_bf16* W, const lmhead_bf16* h, const int32_t* ids,
+                         int64_t n, int d, int M, int K, float* out_logits,
+                         lmhead_stream stream);
+
+/*
+ * Draft distribution over each row's candidates: q[m,j] = exp((L[m,j] -
+ * max_j L[m,:]) / temperature) / sum. The drafter samples its next token
+ * from this distribution (EAGLE -> EAGLE-2 -> EAGLE-3 -> DFlash overview,
+ * course.zhidx.com, section 1.3; the accept/reject rule of "Speculative
+ * decoding and EAGLE", ai-engineering.com.cn, consumes it). Tokens that are
+ * not candidates have probability 0. temperature > 0. out_q may alias logits.
+ */
+int lmhead_candidate_softmax(const float* logits, int M, int K, float temperature,
+                             float* out_q, lmhead_stream stream);
+
+/*
+ * The whole two-stage head in one call: projection, selection (mode as in
+ * lmhead_lowrank_score_topk), gather of W[ids], exact logits and softmax.
+ * Outputs: out_ids, out_logits, out_q, each M x K (K from
+ * lmhead_candidate_count). No host synchronisation.
+ */
+int lmhead_two_stage(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
+                     const lmhead_bf16* B, const lmhead_bf16* h, const int32_t* token_ids,
+                     int64_t n, int d, int r, int M, int C_or_tile, int k_tile,
+                     float temperature, int32_t* out_ids, float* out_logits, float* out_q,
+                     void* workspace, size_t workspace_bytes, lmhead_stream stream);
+
+/*
+ * Comparison head: the dense full-vocabulary head whose cost the method
+ * avoids (EAGLE-4 notes, "EAGLE Efficient LM Head": the LM head can be about
+ * half of a one-layer drafter's forward).
+ *   out_logits M x n fp32 = h W^T; out_q M x n softmax over the whole
+ *   vocabulary, or NULL for logits only.
+ */
+int lmhead_dense_head(const lmhead_bf16* W, const lmhead_bf16* h, int64_t n, int d, int M,
+                      float temperature, float* out_logits, float* out_q,
+                      lmhead_stream stream);
+
+/*
+ * Comparison head: the frequency-pruned vocabulary (FR-Spec style, 32000
+ * most frequent tokens in the EAGLE-4 notes, "EAGLE Efficient LM Head").
+ *   W_pruned  n_keep x d bf16: the kept rows of W, copied contiguously by the
+ *             caller in the order of its kept-id list.
+ *   out_logits, out_q  M x n_keep fp32 over the kept tokens (out_q may be NULL).
+ */
+int lmhead_pruned_head(const lmhead_bf16* W_pruned, const lmhead_bf16* h, int n_keep,
+                       int d, int M, float temperature, float* out_logits, float* out_q,
+                       lmhead_stream stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word. Returns LMHEAD_OK, LMHEAD_ERR_DEVICE_CHECK, LMHEAD_ERR_TIMEOUT, or
+ * LMHEAD_ERR_CUDA if the synchronisation itself failed.
+ */
+int lmhead_last_device_error(lmhead_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMHEAD_H */

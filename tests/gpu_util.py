@@ -1,0 +1,60 @@
+"""Helpers shared by the GPU tests: building the library, moving seeded
+inputs to the device, and running the oracle on the same bits."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+
+import oracle as O
+import synth
+
+
+@functools.lru_cache(maxsize=None)
+def lib():
+    import torch
+    if not torch.cuda.is_available():
+        raise RuntimeError("GPU tests need CUDA")
+    from draft_lm_head_gb300 import build
+    build.build()
+    import draft_lm_head_gb300 as L
+    L.load() if hasattr(L, "load") else None
+    return L
+
+
+def dev_bf16(bits: np.ndarray):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def dev_i32(x: np.ndarray):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).cuda()
+
+
+def host(t) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+def make_case(n, d, r, M, seed, shuffle=True, zipf_s=1.1, plain_h=False):
+    """A seeded synthetic head and its Freq-aware SVD factors (host, bits)."""
+    from draft_lm_head_gb300 import prep
+    W = synth.make_head(n, d, seed)
+    counts = synth.zipf_counts(n, zipf_s, seed)
+    perm = synth.shuffle_perm(n, seed) if shuffle else None
+    fac = prep.freq_aware_factors(W, counts, r, perm)
+    if plain_h:
+        h = synth.make_plain_hidden(d, M, seed)
+    else:
+        h, _ = synth.make_hidden(W, M, seed)
+    return {"W": W, "A": fac["A"], "B": fac["B"], "tok": fac["token_ids"], "h": h,
+            "counts": counts, "n": n, "d": d, "r": r, "M": M}
+
+
+def oracle_scores(case):
+    """Oracle u (bf16 grid, fp64) and position-ordered scores M x n."""
+    A64 = O.bf16_bits_to_f64(case["A"])
+    B64 = O.bf16_bits_to_f64(case["B"])
+    h64 = O.bf16_bits_to_f64(case["h"])
+    u = O.project_u(B64, h64)
+    return u, O.lowrank_scores(A64, u), h64

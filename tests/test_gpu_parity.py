@@ -1,0 +1,224 @@
+"""CUDA path vs the fp64 oracle on small seeded heads (several tiles, ragged
+tails, edge cases), through the C ABI. Full-size workloads are in
+test_gpu_workloads.py."""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+
+from gpu_util import dev_bf16, dev_i32, host, lib, make_case, oracle_scores
+import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    return lib()
+
+
+@pytest.fixture(scope="module")
+def small():
+    return make_case(1000, 64, 16, 17, seed=11)
+
+
+def _dev(case):
+    return (dev_bf16(case["W"]), dev_bf16(case["A"]), dev_bf16(case["B"]),
+            dev_bf16(case["h"]), dev_i32(case["tok"]))
+
+
+def _u_ok(gpu_u_bits, case):
+    """u equals the oracle's bf16 value, or is its neighbour when the exact
+    value lies within the fp32 accumulation error of the rounding midpoint."""
+    B64 = O.bf16_bits_to_f64(case["B"])
+    h64 = O.bf16_bits_to_f64(case["h"])
+    exact = h64 @ B64.T
+    ora = O.project_u(B64, h64)
+    got = O.bf16_bits_to_f64(gpu_u_bits)
+    diff = got != ora
+    if not diff.any():
+        return 0
+    err_bound = case["d"] * 2.0 ** -23 * (np.abs(h64) @ np.abs(B64).T)
+    mid = (got + ora) / 2
+    assert np.all(np.abs(exact[diff] - mid[diff]) <= err_bound[diff] + 1e-30)
+    return int(diff.sum())
+
+
+def test_project_u(L, small):
+    W, A, B, h, tok = _dev(small)
+    u = L.project_u(B, h)
+    _u_ok(host(u.view(__import__("torch").int16)).view(np.uint16), small)
+
+
+@pytest.mark.parametrize("M", [1, 3, 17])
+@pytest.mark.parametrize("T,k", [(128, 1), (128, 2), (128, 4), (100, 32), (7, 3), (1000, 16),
+                                 (4096, 8), (128, 40), (300, 300)])
+def test_local_select(L, small, M, T, k):
+    case = dict(small)
+    case["h"] = small["h"][:M]
+    W, A, B, h, tok = _dev(case)
+    ids, sc = L.lowrank_score_topk(L.LOCAL, A, B, h, tok, T, k, with_scores=True)
+    _, S, _ = oracle_scores(case)
+    P.check_ids("local", host(ids), S, case["tok"], T, k)
+    P.check_order("local", host(ids), host(sc), T, k, case["n"])
+    assert ids.shape[1] == O.local_candidate_count(case["n"], T, k)
+
+
+@pytest.mark.parametrize("M", [1, 5])
+@pytest.mark.parametrize("C", [1, 64, 777, 1000])
+def test_global_select(L, small, M, C):
+    case = dict(small)
+    case["h"] = small["h"][:M]
+    W, A, B, h, tok = _dev(case)
+    ids, sc = L.lowrank_score_topk(L.GLOBAL, A, B, h, tok, C, with_scores=True)
+    _, S, _ = oracle_scores(case)
+    P.check_ids("global", host(ids), S, case["tok"], C)
+    P.check_order("global", host(ids), host(sc), C, 0, case["n"])
+
+
+def test_global_select_long_rows(L):
+    # rows long enough for the multi-pass radix path (> 8192 keys)
+    case = make_case(20000, 64, 16, 3, seed=12)
+    W, A, B, h, tok = _dev(case)
+    _, S, _ = oracle_scores(case)
+    for C in (1, 100, 1024, 4096):
+        ids = L.lowrank_score_topk(L.GLOBAL, A, B, h, tok, C)
+        P.check_ids("global", host(ids), S, case["tok"], C)
+
+
+def test_scores_match_oracle(L, small):
+    W, A, B, h, tok = _dev(small)
+    ids, sc = L.lowrank_score_topk(L.LOCAL, A, B, h, tok, 128, 4, with_scores=True)
+    _, S, _ = oracle_scores(small)
+    ids, sc = host(ids), host(sc)
+    A64 = O.bf16_bits_to_f64(small["A"])
+    inv = np.empty(small["n"], dtype=np.int64)
+    inv[small["tok"]] = np.arange(small["n"])
+    u = O.project_u(O.bf16_bits_to_f64(small["B"]), O.bf16_bits_to_f64(small["h"]))
+    for m in range(ids.shape[0]):
+        pos = inv[ids[m]]
+        bound = 1e-5 * (np.abs(A64[pos]) @ np.abs(u[m])) + 1e-6
+        assert np.all(np.abs(sc[m] - S[m, pos]) <= bound)
+
+
+@pytest.mark.parametrize("mode,C,k", [("local", 128, 2), ("local", 64, 40), ("global", 300, 0)])
+@pytest.mark.parametrize("temp", [1.0, 0.37])
+def test_two_stage(L, mode, C, k, temp):
+    case = make_case(1500, 128, 24, 6, seed=13, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    md = L.LOCAL if mode == "local" else L.GLOBAL
+    ids, lg, q = L.two_stage(md, W, A, B, h, tok, C, k, temperature=temp)
+    _, S, h64 = oracle_scores(case)
+    ids = host(ids)
+    P.check_ids(mode, ids, S, case["tok"], C, k)
+    ex = P.exact_logits(case["W"], h64, ids)
+    P.check_logits(host(lg), ex)
+    P.check_q(host(q), ex, temp)
+
+
+def test_two_stage_identity_token_ids(L):
+    case = make_case(1024, 64, 16, 2, seed=14, shuffle=False)
+    W, A, B, h, _ = _dev(case)
+    ids, lg, q = L.two_stage(L.LOCAL, W, A, B, h, None, 128, 4)
+    _, S, h64 = oracle_scores(case)
+    P.check_ids("local", host(ids), S, np.arange(1024), 128, 4)
+    ex = P.exact_logits(case["W"], h64, host(ids))
+    P.check_logits(host(lg), ex)
+    P.check_q(host(q), ex)
+
+
+def test_unit_tiles_cover_vocabulary(L):
+    case = make_case(300, 32, 8, 2, seed=15, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    ids, lg, q = L.two_stage(L.LOCAL, W, A, B, h, tok, 1, 1)
+    ids = host(ids)
+    assert np.array_equal(ids[0], case["tok"]) and np.array_equal(ids[1], case["tok"])
+    h64 = O.bf16_bits_to_f64(case["h"])
+    Z = O.dense_logits(O.bf16_bits_to_f64(case["W"]), h64)
+    for m in range(2):
+        want = O.candidate_softmax(Z[m])[case["tok"]]
+        assert np.abs(host(q)[m] - want).max() < P.Q_ABS
+
+
+def test_one_tile_equals_global(L, small):
+    W, A, B, h, tok = _dev(small)
+    g = host(L.lowrank_score_topk(L.GLOBAL, A, B, h, tok, 16))
+    l = host(L.lowrank_score_topk(L.LOCAL, A, B, h, tok, small["n"], 16))
+    assert np.array_equal(g, l)
+
+
+def test_gather_logits_and_bad_id(L, small):
+    import torch
+    W, A, B, h, tok = _dev(small)
+    rng = np.random.default_rng(5)
+    ids = rng.integers(0, small["n"], size=(small["M"], 37)).astype(np.int32)
+    ids[0, :3] = [0, small["n"] - 1, 0]
+    got = host(L.gather_logits(W, h, dev_i32(ids)))
+    h64 = O.bf16_bits_to_f64(small["h"])
+    P.check_logits(got, P.exact_logits(small["W"], h64, ids))
+    assert L.last_device_error() == 0
+    bad = ids.copy()
+    bad[1, 5] = small["n"]
+    bad[2, 0] = -1
+    got = host(L.gather_logits(W, h, dev_i32(bad)))
+    assert np.isnan(got[1, 5]) and np.isnan(got[2, 0])
+    assert np.isfinite(np.delete(got.ravel(), [1 * 37 + 5, 2 * 37])).all()
+    assert L.last_device_error() == -7   # LMHEAD_ERR_DEVICE_CHECK, then cleared
+    assert L.last_device_error() == 0
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("K", [1, 5, 1002, 70000])
+@pytest.mark.parametrize("temp", [1.0, 3.0])
+def test_candidate_softmax(L, K, temp):
+    import torch
+    x = np.random.default_rng(K).standard_normal((3, K)).astype(np.float32) * 6
+    q = host(L.candidate_softmax(torch.from_numpy(x).cuda(), temp))
+    for m in range(3):
+        assert np.abs(q[m] - O.candidate_softmax(x[m].astype(np.float64), temp)).max() < P.Q_ABS
+    # aliasing the output onto the input is allowed
+    t = torch.from_numpy(x).cuda()
+    L.candidate_softmax(t, temp, out=t)
+    assert np.abs(host(t) - q).max() < 1e-6
+
+
+@pytest.mark.parametrize("M", [1, 9])
+def test_dense_and_pruned_head(L, M):
+    case = make_case(700, 64, 16, M, seed=16, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    lg, q = L.dense_head(W, h, 0.8)
+    h64 = O.bf16_bits_to_f64(case["h"])
+    Z = O.dense_logits(O.bf16_bits_to_f64(case["W"]), h64)
+    P.check_logits(host(lg), Z)
+    for m in range(M):
+        assert np.abs(host(q)[m] - O.candidate_softmax(Z[m], 0.8)).max() < P.Q_ABS
+    keep = O.pruned_ids(O.smooth_freq(case["counts"]), 200)
+    Wp = dev_bf16(case["W"][keep])
+    lp, qp = L.pruned_head(Wp, h)
+    P.check_logits(host(lp), Z[:, keep])
+    for m in range(M):
+        assert np.abs(host(qp)[m] - O.candidate_softmax(Z[m, keep])).max() < P.Q_ABS
+
+
+def test_deterministic_repeats(L, small):
+    W, A, B, h, tok = _dev(small)
+    outs = [tuple(host(t) for t in L.two_stage(L.LOCAL, W, A, B, h, tok, 128, 4)) for _ in range(3)]
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            assert np.array_equal(a, b)
+
+
+def test_host_validation_errors(L, small):
+    import torch
+    W, A, B, h, tok = _dev(small)
+    with pytest.raises(L.LmheadError) as e:
+        L.two_stage(L.LOCAL, W, A, B, h, tok, 4, 8)       # k_tile > T
+    assert e.value.status == -2
+    with pytest.raises(L.LmheadError) as e:
+        L.two_stage(L.GLOBAL, W, A, B, h, tok, small["n"] + 1)
+    assert e.value.status == -2
+    tiny = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(L.LmheadError) as e:
+        L.two_stage(L.GLOBAL, W, A, B, h, tok, 64, workspace=tiny)
+    assert e.value.status == -4
