@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Benchmark of the two-stage draft LM head on one GB300 (or N replicas).
+
+Workload: the Llama-3-8B-shaped head (n=128256, d=4096, r=256) with rows
+shuffled by a seeded permutation and the fused local Top-k (tile=256,
+k_tile=2 -> 1002 candidates per hidden vector), M hidden vectors per call.
+A step is one lmhead_two_stage call: projection, fused score + tile top-k,
+gather of W[ids], exact logits, softmax. Inputs are synthetic and seeded
+(see synth/), resident in HBM before timing; 4 rotating copies of every
+input (> 2x the 129 MB L2) keep each step's reads cold.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--M 64] [--impl ours|reference]
+
+Prints one JSON line. Under torchrun (N > 1) every rank runs an independent
+replica on its own hidden vectors (no collective on the data path) and rank
+0 prints the aggregate over ranks with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "two-stage LM-head hidden vecs/s (n=128256,d=4096,r=256); % of HBM roofline"
+WORKLOAD = synth.workload(2)
+NROT = 4
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--M", type=int, default=64)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- inputs
+def head_inputs(wl=WORKLOAD):
+    """Seeded head + its Freq-aware SVD factors (offline prep, cached on disk),
+    with the factor rows shuffled by the workload's permutation."""
+    from draft_lm_head_gb300 import prep
+
+    def builder():
+        W = synth.make_head(wl.n, wl.d, wl.head_seed_index)
+        counts = synth.zipf_counts(wl.n, wl.zipf_s, wl.head_seed_index)
+        fac = prep.freq_aware_factors(W, counts, wl.r)
+        return {"W": W, "counts": counts, "A": fac["A"], "B": fac["B"]}
+
+    key = f"head:{wl.head_seed_index}:{wl.n}:{wl.d}:{wl.r}:{wl.zipf_s}"
+    head = dict(synth.head_cache(key, builder))
+    tok = synth.shuffle_perm(wl.n, wl.index) if wl.shuffle else np.arange(wl.n, dtype=np.int32)
+    head["A"] = np.ascontiguousarray(head["A"][tok])
+    head["tok"] = tok
+    return head
+
+
+def hidden(W, M, rank):
+    h, _ = synth.make_hidden(W, M, WORKLOAD.index, stream_offset=rank)
+    return h
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            pk = json.load(fh)
+        return float(pk["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample_rate(head, h_bits, budget_s=12.0, rows=4):
+    """Time the oracle as it stands on `rows` hidden vectors of the workload,
+    repeated for about `budget_s`; returns (vecs/s, cores, sample text)."""
+    import oracle as O
+    wl = WORKLOAD
+    A64 = O.bf16_bits_to_f64(head["A"])
+    B64 = O.bf16_bits_to_f64(head["B"])
+    tok = head["tok"]
+    h64 = O.bf16_bits_to_f64(h_bits[:rows])
+
+    def one_pass():
+        u = O.project_u(B64, h64)
+        S = O.lowrank_scores(A64, u)
+        for m in range(rows):
+            ids, _ = O.local_topk(S[m], tok, wl.T, wl.k_tile)
+            Wr = O.bf16_bits_to_f64(head["W"][ids])
+            L = O.candidate_logits(Wr, h64[m], np.arange(ids.size))
+            O.candidate_softmax(L)
+
+    done, t0 = 0, time.perf_counter()
+    while True:
+        one_pass()
+        done += rows
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return done / dt, cores, f"{done} hidden vectors ({rows} per pass) of the M={rows} slice, {dt:.1f} s"
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from draft_lm_head_gb300 import build
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    import draft_lm_head_gb300 as L
+    L.load()
+
+    wl = WORKLOAD
+    M = args.M
+    head = head_inputs()
+    hb = hidden(head["W"], M, rank)
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    W0, A0, B0 = dev(head["W"]), dev(head["A"]), dev(head["B"])
+    tok0 = torch.from_numpy(head["tok"]).cuda()
+    h0 = dev(hb)
+    rot = [(W0, A0, B0, tok0, h0)] + [(W0.clone(), A0.clone(), B0.clone(), tok0.clone(), h0.clone())
+                                      for _ in range(NROT - 1)]
+    K = L.candidate_count(L.LOCAL, wl.n, wl.T, wl.k_tile)
+    ws = L.Workspace()
+    outs = [(torch.empty((M, K), dtype=torch.int32, device="cuda"),
+             torch.empty((M, K), dtype=torch.float32, device="cuda"),
+             torch.empty((M, K), dtype=torch.float32, device="cuda")) for _ in range(NROT)]
+
+    def step(i, Mx=M, hx=None):
+        Wt, At, Bt, tk, ht = rot[i % NROT]
+        return L.two_stage(L.LOCAL, Wt, At, Bt, ht if hx is None else hx, tk, wl.T, wl.k_tile,
+                           workspace=ws, out=outs[i % NROT] if Mx == M else None)
+
+    sampler = ClockSampler(local)
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * M * args.steps / (ms / 1e3)
+    launches = L.load().lmhead_two_stage_launches(L.LOCAL, wl.k_tile) * args.steps
+
+    # per-kernel durations over the same number of steps (events between launches)
+    nl = L.load().lmhead_two_stage_launches(L.LOCAL, wl.k_tile)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    import ctypes
+    lib = L.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    for i in range(args.steps):
+        Wt, At, Bt, tk, ht = rot[i % NROT]
+        ids, lg, q = outs[i % NROT]
+        handles = (ctypes.c_void_p * (nl + 1))(*[e.cuda_event for e in evs[i]])
+        buf = ws.get(L.workspace_size(L.LOCAL, wl.n, wl.d, wl.r, M, wl.T, wl.k_tile), ids.device)
+        L.check(lib.lmhead_two_stage_profiled(
+            L.LOCAL, Wt.data_ptr(), At.data_ptr(), Bt.data_ptr(), ht.data_ptr(), tk.data_ptr(),
+            wl.n, wl.d, wl.r, M, wl.T, wl.k_tile, 1.0, ids.data_ptr(), lg.data_ptr(), q.data_ptr(),
+            buf.data_ptr(), buf.numel(), handles, nl + 1, stream), "two_stage_profiled")
+    torch.cuda.synchronize()
+    names = ["project_u", "score_local_topk", "gather_logits_softmax"]
+    kern_us = {names[k]: 1e3 * statistics.fmean(evs[i][k].elapsed_time(evs[i][k + 1])
+                                                 for i in range(args.steps)) for k in range(nl)}
+
+    # unique gathered rows -> algorithmic bytes
+    ids_h = outs[0][0].cpu().numpy()
+    U = int(np.unique(ids_h).size)
+    n, d, r = wl.n, wl.d, wl.r
+    bytes_kernel = {
+        "project_u": 2 * r * d + 2 * M * d + 2 * M * r,
+        "score_local_topk": 2 * n * r + 2 * M * r + 4 * M * K,
+        "gather_logits_softmax": 2 * d * U + 2 * M * d + 4 * M * K + 8 * M * K,
+    }
+    step_bytes = 2 * n * r + 2 * r * d + 2 * M * d + 2 * d * U + 12 * M * K
+    hbm, peak_kind = peaks()
+    dom = max(kern_us, key=kern_us.get)
+    achieved = bytes_kernel[dom] / (kern_us[dom] * 1e-6) / 1e9
+    roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
+            "bytes_per_launch": bytes_kernel[dom], "traffic": None}
+
+    # end to end through the public API, host buffers, copies inside the timed region
+    h_host = [torch.from_numpy(np.ascontiguousarray(hb).view(np.int16)).view(torch.bfloat16).pin_memory()
+              for _ in range(NROT)]
+    host_out = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[0])
+                for _ in range(NROT)]
+    h_dev = [torch.empty_like(h0) for _ in range(NROT)]
+
+    def e2e_step(i):
+        j = i % NROT
+        h_dev[j].copy_(h_host[j], non_blocking=True)
+        Wt, At, Bt, tk, _ = rot[j]
+        res = L.two_stage(L.LOCAL, Wt, At, Bt, h_dev[j], tk, wl.T, wl.k_tile, workspace=ws,
+                          out=outs[j])
+        for dst, src in zip(host_out[j], res):
+            dst.copy_(src, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_e2e], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e = {"value": round(world * M * args.steps / (ms_e2e / 1e3), 1), "unit": "hidden vecs/s",
+           "h2d_bytes_per_step": int(hb.nbytes),
+           "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs[0]))}
+
+    # sweep over M and the dense head, for context
+    sweep = []
+    if not args.no_sweep and rank == 0:
+        for Mx in (1, 8, 16, 32, 64):
+            hx_bits = hidden(head["W"], Mx, rank)
+            hx = dev(hx_bits)
+            reps = 30
+            for i in range(3):
+                step(i, Mx, hx)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for i in range(reps):
+                res = step(i, Mx, hx)
+            b.record()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / reps
+            Ux = int(np.unique(res[0].cpu().numpy()).size)
+            by = 2 * n * r + 2 * r * d + 2 * Mx * d + 2 * d * Ux + 12 * Mx * K
+            dl = torch.empty((Mx, n), dtype=torch.float32, device="cuda")
+            dq = torch.empty((Mx, n), dtype=torch.float32, device="cuda")
+            for i in range(2):
+                L.dense_head(rot[i % NROT][0], hx, out=(dl, dq))
+            torch.cuda.synchronize()
+            a.record()
+            for i in range(reps):
+                L.dense_head(rot[i % NROT][0], hx, out=(dl, dq))
+            b.record()
+            torch.cuda.synchronize()
+            dus = a.elapsed_time(b) * 1e3 / reps
+            sweep.append({"M": Mx, "us": round(us, 2), "vecs_per_s": round(Mx / us * 1e6, 1),
+                          "unique_rows": Ux, "bytes": by,
+                          "hbm_frac": round(by / (us * 1e-6) / 1e9 / hbm, 4),
+                          "dense_us": round(dus, 2)})
+    clocks = sampler.stop()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        rate, cores, sample = oracle_sample_rate(head, hb)
+        cpu = {"value": round(rate, 3), "unit": "hidden vecs/s", "cores": cores, "kind": "oracle",
+               "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "hidden vecs/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded rank-64+noise bf16 head, Zipf(1.1) counts, recipe hidden states",
+            "config": {"workload": "llama3-8b-shaped head n=128256 d=4096 r=256, shuffled rows, "
+                                   "fused local top-k tile=256 k_tile=2",
+                       "n": n, "d": d, "r": r, "M": M, "mode": "local", "tile": wl.T,
+                       "k_tile": wl.k_tile, "candidates": K,
+                       "l2": f"{NROT} rotating copies of every input (> 2x L2)",
+                       "parallelism": f"replicas x{world} (independent hidden vectors)"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks, "kernel_us": {k: round(v, 3) for k, v in kern_us.items()},
+            "step_bytes": step_bytes,
+            "step_hbm_frac": round(step_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm, 4),
+            "unique_rows": U, "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if rank != 0:
+        return
+    import oracle as O
+    wl = WORKLOAD
+    rows = 8
+    head = head_inputs()
+    hb = hidden(head["W"], rows, 0)
+    A64 = O.bf16_bits_to_f64(head["A"])
+    B64 = O.bf16_bits_to_f64(head["B"])
+    h64 = O.bf16_bits_to_f64(hb)
+
+    def step():
+        u = O.project_u(B64, h64)
+        S = O.lowrank_scores(A64, u)
+        for m in range(rows):
+            ids, _ = O.local_topk(S[m], head["tok"], wl.T, wl.k_tile)
+            Lg = O.candidate_logits(O.bf16_bits_to_f64(head["W"][ids]), h64[m], np.arange(ids.size))
+            O.candidate_softmax(Lg)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "hidden vecs/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded rank-64+noise bf16 head, Zipf(1.1) counts, recipe hidden states",
+        "config": {"workload": "llama3-8b-shaped head n=128256 d=4096 r=256, shuffled rows, "
+                               "fused local top-k tile=256 k_tile=2",
+                   "n": wl.n, "d": wl.d, "r": wl.r, "M": rows, "mode": "local", "tile": wl.T,
+                   "k_tile": wl.k_tile},
+        "cpu_baseline": {"value": round(value, 3), "unit": "hidden vecs/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{rows} hidden vectors per step of the workload, fp64 NumPy oracle"},
+        "e2e": {"value": round(value, 3), "unit": "hidden vecs/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -26,6 +26,9 @@ SIGNATURES = {
     "lmhead_candidate_softmax": (_I, [_P, _I, _I, _F, _P, _P]),
     "lmhead_two_stage": (_I, [_I, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _F,
                               _P, _P, _P, _P, _SZ, _P]),
+    "lmhead_two_stage_profiled": (_I, [_I, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _F,
+                                       _P, _P, _P, _P, _SZ, _P, _I, _P]),
+    "lmhead_two_stage_launches": (_I, [_I, _I]),
     "lmhead_dense_head": (_I, [_P, _P, _I64, _I, _I, _F, _P, _P, _P]),
     "lmhead_pruned_head": (_I, [_P, _P, _I, _I, _I, _F, _P, _P, _P]),
     "lmhead_last_device_error": (_I, [_P]),

@@ -85,27 +85,48 @@ int check_select(int mode, int64_t n, int d, int r, int M, int C_or_tile, int k_
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? LMHEAD_OK : LMHEAD_ERR_CUDA; }
 
+// Optional timing marks between launches (lmhead_two_stage_profiled).
+struct Marks {
+  void* const* events = nullptr;
+  int n = 0;
+  int next = 0;
+  cudaError_t mark(cudaStream_t s) {
+    if (next < n && events && events[next]) {
+      cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[next]), s);
+      ++next;
+      return e;
+    }
+    ++next;
+    return cudaSuccess;
+  }
+};
+
 // Stage 1 on validated arguments; u lives in the workspace.
 int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
                const int32_t* token_ids, int64_t n, int d, int r, int M, int C_or_tile,
                int k_tile, int32_t* out_ids, float* out_scores, char* ws, const Layout& L,
-               bool zero_tickets, cudaStream_t s) {
+               bool zero_tickets, Marks& mk, cudaStream_t s) {
   bf16_t* u = reinterpret_cast<bf16_t*>(ws + L.u);
   int* tickets = reinterpret_cast<int*>(ws + L.tickets);
+  if (mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   cudaError_t e = launch_project_u(B, h, d, r, M, u, zero_tickets ? tickets : nullptr, M, s);
-  if (e != cudaSuccess) return LMHEAD_ERR_CUDA;
+  if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   if (!needs_score_buffer(mode, k_tile)) {
     e = launch_local_topk_fma(A, u, token_ids, n, r, M, C_or_tile, k_tile, out_ids, out_scores, s);
-    return cuda_status(e);
+    if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
+    return LMHEAD_OK;
   }
   float* S = reinterpret_cast<float*>(ws + L.scores);
   e = launch_score_all_fma(A, u, n, r, M, S, s);
-  if (e != cudaSuccess) return LMHEAD_ERR_CUDA;
+  if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   const int64_t seg = mode == LMHEAD_GLOBAL ? n : C_or_tile;
   const int k = mode == LMHEAD_GLOBAL ? C_or_tile : k_tile;
   e = launch_segment_topk(S, token_ids, n, M, seg, k, out_ids, out_scores, device_error_word(), s);
-  return cuda_status(e);
+  if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
+  return LMHEAD_OK;
 }
+
+int launches_for(int mode, int k_tile) { return needs_score_buffer(mode, k_tile) ? 4 : 3; }
 
 bool valid_temperature(float t) { return t > 0.f && isfinite(t); }
 
@@ -167,8 +188,9 @@ int lmhead_lowrank_score_topk(int mode, const lmhead_bf16* A, const lmhead_bf16*
   const Layout L = layout_for(mode, n, r, M, k_tile);
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return LMHEAD_ERR_WORKSPACE;
+  Marks none;
   return run_select(mode, A, B, h, token_ids, n, d, r, M, C_or_tile, k_tile, out_ids, out_scores,
-                    static_cast<char*>(workspace), L, false, (cudaStream_t)stream);
+                    static_cast<char*>(workspace), L, false, none, (cudaStream_t)stream);
 }
 
 int lmhead_gather_logits(const lmhead_bf16* W, const lmhead_bf16* h, const int32_t* ids,
@@ -192,11 +214,12 @@ int lmhead_candidate_softmax(const float* logits, int M, int K, float temperatur
                                         (cudaStream_t)stream));
 }
 
-int lmhead_two_stage(int mode, const lmhead_bf16* W, const lmhead_bf16* A, const lmhead_bf16* B,
-                     const lmhead_bf16* h, const int32_t* token_ids, int64_t n, int d, int r,
-                     int M, int C_or_tile, int k_tile, float temperature, int32_t* out_ids,
-                     float* out_logits, float* out_q, void* workspace, size_t workspace_bytes,
-                     lmhead_stream stream) {
+static int two_stage_impl(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
+                          const lmhead_bf16* B, const lmhead_bf16* h, const int32_t* token_ids,
+                          int64_t n, int d, int r, int M, int C_or_tile, int k_tile,
+                          float temperature, int32_t* out_ids, float* out_logits, float* out_q,
+                          void* workspace, size_t workspace_bytes, Marks& mk,
+                          lmhead_stream stream) {
   if (!W || !A || !B || !h || !out_ids || !out_logits || !out_q) return LMHEAD_ERR_NULL;
   if (mode == LMHEAD_GLOBAL) k_tile = 0;
   int st = check_select(mode, n, d, r, M, C_or_tile, k_tile);
@@ -211,13 +234,44 @@ int lmhead_two_stage(int mode, const lmhead_bf16* W, const lmhead_bf16* A, const
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = (cudaStream_t)stream;
   st = run_select(mode, A, B, h, token_ids, n, d, r, M, C_or_tile, k_tile, out_ids, nullptr, ws,
-                  L, true, s);
+                  L, true, mk, s);
   if (st != LMHEAD_OK) return st;
   const int K = (int)candidate_count(mode, n, C_or_tile, k_tile);
-  return cuda_status(launch_gather_logits(W, h, out_ids, n, d, M, K, out_logits, out_q,
-                                          1.f / temperature,
-                                          reinterpret_cast<int*>(ws + L.tickets),
-                                          device_error_word(), s));
+  cudaError_t e = launch_gather_logits(W, h, out_ids, n, d, M, K, out_logits, out_q,
+                                       1.f / temperature, reinterpret_cast<int*>(ws + L.tickets),
+                                       device_error_word(), s);
+  if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
+  return LMHEAD_OK;
+}
+
+int lmhead_two_stage(int mode, const lmhead_bf16* W, const lmhead_bf16* A, const lmhead_bf16* B,
+                     const lmhead_bf16* h, const int32_t* token_ids, int64_t n, int d, int r,
+                     int M, int C_or_tile, int k_tile, float temperature, int32_t* out_ids,
+                     float* out_logits, float* out_q, void* workspace, size_t workspace_bytes,
+                     lmhead_stream stream) {
+  Marks none;
+  return two_stage_impl(mode, W, A, B, h, token_ids, n, d, r, M, C_or_tile, k_tile, temperature,
+                        out_ids, out_logits, out_q, workspace, workspace_bytes, none, stream);
+}
+
+int lmhead_two_stage_profiled(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
+                              const lmhead_bf16* B, const lmhead_bf16* h,
+                              const int32_t* token_ids, int64_t n, int d, int r, int M,
+                              int C_or_tile, int k_tile, float temperature, int32_t* out_ids,
+                              float* out_logits, float* out_q, void* workspace,
+                              size_t workspace_bytes, void* const* events, int n_events,
+                              lmhead_stream stream) {
+  if (n_events < 0 || (n_events > 0 && !events)) return LMHEAD_ERR_NULL;
+  Marks mk;
+  mk.events = events;
+  mk.n = n_events;
+  return two_stage_impl(mode, W, A, B, h, token_ids, n, d, r, M, C_or_tile, k_tile, temperature,
+                        out_ids, out_logits, out_q, workspace, workspace_bytes, mk, stream);
+}
+
+int lmhead_two_stage_launches(int mode, int k_tile) {
+  if (mode == LMHEAD_GLOBAL) k_tile = 0;
+  return launches_for(mode, k_tile);
 }
 
 int lmhead_dense_head(const lmhead_bf16* W, const lmhead_bf16* h, int64_t n, int d, int M,

@@ -160,6 +160,22 @@ int lmhead_two_stage(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
                      void* workspace, size_t workspace_bytes, lmhead_stream stream);
 
 /*
+ * lmhead_two_stage with timing marks for profiling: records events[0] on
+ * `stream` before the first kernel and events[i] after the i-th kernel
+ * launch, for i < n_events (events are cudaEvent_t created by the caller).
+ * lmhead_two_stage_launches gives the number of kernels a call launches.
+ * Same arguments, outputs and errors as lmhead_two_stage otherwise.
+ */
+int lmhead_two_stage_profiled(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
+                              const lmhead_bf16* B, const lmhead_bf16* h,
+                              const int32_t* token_ids, int64_t n, int d, int r, int M,
+                              int C_or_tile, int k_tile, float temperature, int32_t* out_ids,
+                              float* out_logits, float* out_q, void* workspace,
+                              size_t workspace_bytes, void* const* events, int n_events,
+                              lmhead_stream stream);
+int lmhead_two_stage_launches(int mode, int k_tile);
+
+/*
  * Comparison head: the dense full-vocabulary head whose cost the method
  * avoids (EAGLE-4 notes, "EAGLE Efficient LM Head": the LM head can be about
  * half of a one-layer drafter's forward).

@@ -51,6 +51,34 @@ def make_case(n, d, r, M, seed, shuffle=True, zipf_s=1.1, plain_h=False):
             "counts": counts, "n": n, "d": d, "r": r, "M": M}
 
 
+def workload_head(wl):
+    """The seeded head of a workload with its Freq-aware SVD factors in
+    vocabulary order (cached under _cache/); rows are shuffled per use."""
+    from draft_lm_head_gb300 import prep
+
+    def builder():
+        W = synth.make_head(wl.n, wl.d, wl.head_seed_index)
+        counts = synth.zipf_counts(wl.n, wl.zipf_s, wl.head_seed_index)
+        fac = prep.freq_aware_factors(W, counts, wl.r)
+        return {"W": W, "counts": counts, "A": fac["A"], "B": fac["B"]}
+
+    key = f"head:{wl.head_seed_index}:{wl.n}:{wl.d}:{wl.r}:{wl.zipf_s}"
+    return synth.head_cache(key, builder)
+
+
+def workload_case(wl, M, shuffle=None, tree=None, stream_offset=0):
+    head = workload_head(wl)
+    shuffle = wl.shuffle if shuffle is None else shuffle
+    tok = synth.shuffle_perm(wl.n, wl.index) if shuffle else np.arange(wl.n, dtype=np.int32)
+    tree = wl.tree if tree is None else tree
+    if tree:
+        h, t = synth.make_tree_hidden(head["W"], M // len(synth.TREE_PARENT), wl.index)
+    else:
+        h, t = synth.make_hidden(head["W"], M, wl.index, stream_offset)
+    return {"W": head["W"], "A": np.ascontiguousarray(head["A"][tok]), "B": head["B"], "tok": tok,
+            "h": h, "t": t, "counts": head["counts"], "n": wl.n, "d": wl.d, "r": wl.r, "M": M}
+
+
 def oracle_scores(case):
     """Oracle u (bf16 grid, fp64) and position-ordered scores M x n."""
     A64 = O.bf16_bits_to_f64(case["A"])

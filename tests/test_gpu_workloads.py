@@ -1,0 +1,153 @@
+"""CUDA path vs the fp64 oracle on the five seeded workloads at full size,
+through the C ABI, in the launch configuration the bench times.
+
+Workloads (seeded, synthetic; see synth/):
+  0  n=4096   d=256  r=32,  M=1: global C=128; local tile 128, k_tile 4 (shuffled and identity)
+  1  n=128256 d=4096 r=256, M in {1,4,8}: global C=1024 (identity order)
+  2  same head, shuffled, M in {1,8,16,32,64}: local tile 256, k_tile 2 (1002 candidates);
+     global C=1002 and 1024 for the recall comparison
+  3  n=201088 d=2880 r=256, M=80 (8 sequences x 10-node tree): local 256/2; global C=1024
+  4  n=151936 d=5120 r=512, M in {1,8,32,128,512}: local 256/4; dense; pruned 32000
+Recall of the exact full-head Top-{1,8,64} is written to gpurun_out/recall_*.json
+when that folder exists (a report, not a pass/fail criterion).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+
+from gpu_util import dev_bf16, dev_i32, host, lib, oracle_scores, workload_case
+import parity as P
+
+pytestmark = pytest.mark.gpu
+
+OUT = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
+
+
+@pytest.fixture(scope="module")
+def L():
+    return lib()
+
+
+def _run(L, case, mode, C, k, rows=None):
+    W, A, B = dev_bf16(case["W"]), dev_bf16(case["A"]), dev_bf16(case["B"])
+    h, tok = dev_bf16(case["h"]), dev_i32(case["tok"])
+    md = L.LOCAL if mode == "local" else L.GLOBAL
+    ids, lg, q = L.two_stage(md, W, A, B, h, tok, C, k)
+    assert L.last_device_error() == 0
+    return host(ids), host(lg), host(q)
+
+
+def _check(case, mode, C, k, ids, lg, q, rows=None):
+    rows = np.arange(case["M"]) if rows is None else np.asarray(rows)
+    sub = dict(case)
+    sub["h"] = case["h"][rows]
+    _, S, h64 = oracle_scores(sub)
+    excused = P.check_ids(mode, ids[rows], S, case["tok"], C, k)
+    ex = P.exact_logits(case["W"], h64, ids[rows])
+    floor = P.check_logits(lg[rows], ex)
+    P.check_q(q[rows], ex)
+    return excused, floor
+
+
+def _dense_exact(W_bits, h64, block=16384):
+    Z = np.empty((h64.shape[0], W_bits.shape[0]))
+    for r0 in range(0, W_bits.shape[0], block):
+        Z[:, r0:r0 + block] = h64 @ O.bf16_bits_to_f64(W_bits[r0:r0 + block]).T
+    return Z
+
+
+def _report(name, payload):
+    if os.path.isdir(OUT):
+        with open(os.path.join(OUT, f"recall_{name}.json"), "w") as fh:
+            json.dump(payload, fh, indent=1)
+    print(name, json.dumps(payload))
+
+
+def test_workload0_tiny(L):
+    wl = synth.workload(0)
+    for shuffle in (True, False):
+        case = workload_case(wl, 1, shuffle=shuffle)
+        ids, lg, q = _run(L, case, "local", wl.T, wl.k_tile)
+        assert ids.shape == (1, 128)
+        _check(case, "local", wl.T, wl.k_tile, ids, lg, q)
+    case = workload_case(wl, 1)
+    ids, lg, q = _run(L, case, "global", wl.C, 0)
+    _check(case, "global", wl.C, 0, ids, lg, q)
+
+
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_workload1_global(L, M):
+    wl = synth.workload(1)
+    case = workload_case(wl, M)
+    ids, lg, q = _run(L, case, "global", wl.C, 0)
+    assert ids.shape == (M, 1024)
+    _check(case, "global", wl.C, 0, ids, lg, q)
+
+
+@pytest.mark.parametrize("M", [1, 8, 16, 32, 64])
+def test_workload2_local(L, M):
+    wl = synth.workload(2)
+    case = workload_case(wl, M)
+    ids, lg, q = _run(L, case, "local", wl.T, wl.k_tile)
+    assert ids.shape == (M, 1002)
+    _check(case, "local", wl.T, wl.k_tile, ids, lg, q)
+    if M == 64:
+        h64 = O.bf16_bits_to_f64(case["h"])
+        Z = _dense_exact(case["W"], h64)
+        g1002, _, _ = _run(L, case, "global", 1002, 0)
+        g1024, _, _ = _run(L, case, "global", 1024, 0)
+        rep = {}
+        for name, cand in (("local_1002", ids), ("global_1002", g1002), ("global_1024", g1024)):
+            rep[name] = {f"recall@{k}": float(np.mean([O.recall_at(cand[m], Z[m], k) for m in range(M)]))
+                         for k in (1, 8, 64)}
+        _report("workload2", rep)
+        assert rep["local_1002"]["recall@1"] > 0.9
+
+
+def test_workload3_tree(L):
+    wl = synth.workload(3)
+    case = workload_case(wl, 80)
+    ids, lg, q = _run(L, case, "local", wl.T, wl.k_tile)
+    assert ids.shape == (80, 1572)
+    _check(case, "local", wl.T, wl.k_tile, ids, lg, q)
+    gi, gl, gq = _run(L, case, "global", wl.C, 0)
+    _check(case, "global", wl.C, 0, gi, gl, gq, rows=[0, 1, 9, 37, 79])
+    h64 = O.bf16_bits_to_f64(case["h"][:16])
+    Z = _dense_exact(case["W"], h64)
+    rep = {name: {f"recall@{k}": float(np.mean([O.recall_at(c[m], Z[m], k) for m in range(16)]))
+                  for k in (1, 8, 64)} for name, c in (("local_1572", ids), ("global_1024", gi))}
+    _report("workload3", rep)
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 128, 512])
+def test_workload4_wide(L, M):
+    wl = synth.workload(4)
+    case = workload_case(wl, M)
+    ids, lg, q = _run(L, case, "local", wl.T, wl.k_tile)
+    assert ids.shape == (M, 2376)
+    rows = None if M <= 32 else sorted({0, 1, M // 2, M - 1, *range(7, M, M // 6)})
+    _check(case, "local", wl.T, wl.k_tile, ids, lg, q, rows=rows)
+
+
+@pytest.mark.parametrize("M", [1, 32])
+def test_workload4_dense_and_pruned(L, M):
+    wl = synth.workload(4)
+    case = workload_case(wl, M)
+    W, h = dev_bf16(case["W"]), dev_bf16(case["h"])
+    lg, q = L.dense_head(W, h)
+    rows = [0, M - 1]
+    h64 = O.bf16_bits_to_f64(case["h"][rows])
+    Z = _dense_exact(case["W"], h64)
+    P.check_logits(host(lg)[rows], Z)
+    for i, m in enumerate(rows):
+        assert np.abs(host(q)[m] - O.candidate_softmax(Z[i])).max() < P.Q_ABS
+    keep = O.pruned_ids(O.smooth_freq(case["counts"]), 32000)
+    lp, qp = L.pruned_head(dev_bf16(case["W"][keep]), h)
+    P.check_logits(host(lp)[rows], Z[:, keep])
+    for i, m in enumerate(rows):
+        assert np.abs(host(qp)[m] - O.candidate_softmax(Z[i, keep])).max() < P.Q_ABS
