@@ -198,6 +198,33 @@ int lmhead_pruned_head(const lmhead_bf16* W_pruned, const lmhead_bf16* h, int n_
                        lmhead_stream stream);
 
 /*
+ * Local-mode two-stage head that allocates nothing and takes no workspace.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory or hand over a workspace, such as a
+ * serving engine that gives all free HBM to its KV-cache pool at start-up and
+ * forbids allocation in its decode loop, or C/C++ code embedding the library
+ * with no device allocator of its own. Arguments, outputs and results are
+ * those of lmhead_two_stage with mode = LMHEAD_LOCAL, C_or_tile = T.
+ *   Scratch: a fixed static device array of 513 KiB (u for M <= 256 and
+ *   r <= 1024, plus M per-row counters) held by every GPU that loads the
+ *   library until the process exits. M > 256, r > 1024 or k_tile > 32
+ *   returns LMHEAD_ERR_UNSUPPORTED and enqueues nothing.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the last call's
+ *   contents (the call zeroes what must start at zero). Calls whose work
+ *   overlaps on the GPU (other streams, other host threads) race on the
+ *   array and corrupt each other's outputs: serialise them.
+ *   Never calls cudaMalloc, cudaFree or any allocating library routine.
+ */
+int lmhead_two_stage_local_noalloc(const lmhead_bf16* W, const lmhead_bf16* A,
+                                   const lmhead_bf16* B, const lmhead_bf16* h,
+                                   const int32_t* token_ids, int64_t n, int d, int r, int M,
+                                   int T, int k_tile, float temperature, int32_t* out_ids,
+                                   float* out_logits, float* out_q, lmhead_stream stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * word. Returns LMHEAD_OK, LMHEAD_ERR_DEVICE_CHECK, LMHEAD_ERR_TIMEOUT, or
  * LMHEAD_ERR_CUDA if the synchronisation itself failed.
