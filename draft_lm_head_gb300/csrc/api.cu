@@ -35,20 +35,31 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t u = 0, tickets = 0, scores = 0, total = 0;
+  size_t u = 0, tickets = 0, scores = 0, partials = 0, total = 0;
+  int n_tickets = 0;  // ints at `tickets` zeroed by K1: row tickets then tile tickets
 };
+
+bool use_tc(int mode, int r, int T, int k_tile) {
+  return mode == LMHEAD_LOCAL && local_topk_tc_supported(r, T, k_tile);
+}
 
 bool needs_score_buffer(int mode, int k_tile) {
   return mode == LMHEAD_GLOBAL || k_tile > kFusedMaxKTile;
 }
 
-Layout layout_for(int mode, int64_t n, int r, int M, int k_tile) {
+Layout layout_for(int mode, int64_t n, int r, int M, int C_or_tile, int k_tile) {
   Layout L;
   size_t off = 0;
   L.u = off;
   off = round_up(off + (size_t)M * r * sizeof(bf16_t), 256);
   L.tickets = off;
-  off = round_up(off + (size_t)M * sizeof(int), 256);
+  const bool tc = use_tc(mode, r, C_or_tile, k_tile);
+  L.n_tickets = M + (tc ? local_topk_tc_tickets(n, M, C_or_tile) : 0);
+  off = round_up(off + (size_t)L.n_tickets * sizeof(int), 256);
+  if (tc) {
+    L.partials = off;
+    off = round_up(off + local_topk_tc_scratch_bytes(n, M, C_or_tile), 256);
+  }
   if (needs_score_buffer(mode, k_tile)) {
     L.scores = off;
     off = round_up(off + (size_t)M * (size_t)n * sizeof(float), 256);
@@ -109,8 +120,17 @@ int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
   bf16_t* u = reinterpret_cast<bf16_t*>(ws + L.u);
   int* tickets = reinterpret_cast<int*>(ws + L.tickets);
   if (mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
-  cudaError_t e = launch_project_u(B, h, d, r, M, u, zero_tickets ? tickets : nullptr, M, s);
+  const bool tc = use_tc(mode, r, C_or_tile, k_tile);
+  const bool zero = zero_tickets || tc;
+  cudaError_t e = launch_project_u(B, h, d, r, M, u, zero ? tickets : nullptr,
+                                   zero ? L.n_tickets : 0, s);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
+  if (tc) {
+    e = launch_local_topk_tc(A, u, token_ids, n, r, M, C_or_tile, k_tile, out_ids, out_scores,
+                             ws + L.partials, tickets + M, device_error_word(), s);
+    if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
+    return LMHEAD_OK;
+  }
   if (!needs_score_buffer(mode, k_tile)) {
     e = launch_local_topk_fma(A, u, token_ids, n, r, M, C_or_tile, k_tile, out_ids, out_scores, s);
     if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
@@ -161,7 +181,7 @@ int64_t lmhead_candidate_count(int mode, int64_t n, int C_or_tile, int k_tile) {
 size_t lmhead_workspace_size(int mode, int64_t n, int d, int r, int M, int C_or_tile,
                              int k_tile) {
   if (check_select(mode, n, d, r, M, C_or_tile, k_tile) != LMHEAD_OK) return 0;
-  return layout_for(mode, n, r, M, k_tile).total;
+  return layout_for(mode, n, r, M, C_or_tile, k_tile).total;
 }
 
 int lmhead_project_u(const lmhead_bf16* B, const lmhead_bf16* h, int d, int r, int M,
@@ -185,7 +205,7 @@ int lmhead_lowrank_score_topk(int mode, const lmhead_bf16* A, const lmhead_bf16*
   if (!aligned16(A) || !aligned16(B) || !aligned16(h) || (token_ids && !aligned16(token_ids)) ||
       !aligned16(out_ids) || (out_scores && !aligned16(out_scores)))
     return LMHEAD_ERR_ALIGN;
-  const Layout L = layout_for(mode, n, r, M, k_tile);
+  const Layout L = layout_for(mode, n, r, M, C_or_tile, k_tile);
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return LMHEAD_ERR_WORKSPACE;
   Marks none;
@@ -228,7 +248,7 @@ static int two_stage_impl(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
   if (!aligned16(W) || !aligned16(A) || !aligned16(B) || !aligned16(h) ||
       (token_ids && !aligned16(token_ids)) || !aligned16(out_ids))
     return LMHEAD_ERR_ALIGN;
-  const Layout L = layout_for(mode, n, r, M, k_tile);
+  const Layout L = layout_for(mode, n, r, M, C_or_tile, k_tile);
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return LMHEAD_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);

@@ -15,7 +15,7 @@ constexpr int kFusedMaxKTile = 32;
 constexpr int kSelectMaxK = 4096;
 
 // K1: u = bf16(B h), fp32 accumulation. Also zeroes `zero_ints` ints at
-// `zero_ptr` (per-row tickets of the fused softmax), if non-null.
+// `zero_ptr` (tickets of the fused kernels that follow), if non-null.
 cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int M, bf16_t* u,
                              int* zero_ptr, int zero_ints, cudaStream_t s);
 
@@ -23,6 +23,18 @@ cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int
 cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
                                   int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,
                                   float* out_scores, cudaStream_t s);
+
+// K4 (tensor cores): tcgen05 MMA with TMA-staged A chunks, persistent CTAs.
+constexpr int kLocalTcMaxR = 512;
+constexpr int kLocalTcMaxCtas = 256;
+bool local_topk_tc_supported(int r, int T, int k_tile);
+// workspace bytes for the split-tile partial lists; tile tickets are counted separately
+size_t local_topk_tc_scratch_bytes(int64_t n, int M, int T);
+int local_topk_tc_tickets(int64_t n, int M, int T);
+cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
+                                 int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,
+                                 float* out_scores, void* partials, int* tile_tickets, int* err,
+                                 cudaStream_t s);
 
 // K2 (CUDA cores): S[m, p] = A[p] . u[m] for every position p, fp32 to HBM.
 cudaError_t launch_score_all_fma(const bf16_t* A, const bf16_t* u, int64_t n, int r, int M,

@@ -21,8 +21,9 @@ __global__ void __launch_bounds__(256) project_u_kernel(const bf16_t* __restrict
                                                         int M, bf16_t* __restrict__ u,
                                                         int* zero_ptr, int zero_ints) {
   __shared__ uint4 hs[kMB * kDChunk / 8];
-  if (zero_ptr && blockIdx.x == 0 && blockIdx.y == 0) {
-    for (int i = threadIdx.x; i < zero_ints; i += blockDim.x) zero_ptr[i] = 0;
+  if (zero_ptr) {
+    const int nb = gridDim.x * gridDim.y, bid = blockIdx.y * gridDim.x + blockIdx.x;
+    for (int i = bid * blockDim.x + threadIdx.x; i < zero_ints; i += nb * blockDim.x) zero_ptr[i] = 0;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int k = blockIdx.x * kRowsPerCta + warp;

@@ -1,0 +1,489 @@
+// K4 on the 5th-generation tensor cores: fused low-rank tile scores + local
+// top-k (EAGLE-4 notes, "A Local Top-k based variant": each program scores
+// one vocabulary tile, keeps the scores on chip, picks the tile's top k_tile
+// and writes tile.token_ids[local_ids]; no full-vocabulary score writeback).
+//
+// Design for sm_103a, one persistent CTA per SM:
+//  - The vocabulary is cut into 128-row chunks; CTA b streams a contiguous
+//    range of chunks (balanced over the CTAs). Chunk rows of A (n x r bf16,
+//    row-major = K-major) arrive by TMA as 128-row x 64-element boxes with
+//    the 128-byte swizzle into a ring of shared-memory stages.
+//  - u (128 hidden vectors x r, zero-filled past M) is loaded once by TMA and
+//    is the MMA's A operand; the chunk is the B operand (N = 128). One
+//    elected thread issues tcgen05.mma (M=128, N=128, K=16, fp32 in TMEM)
+//    into two TMEM accumulators, so the epilogue of chunk i overlaps the
+//    MMAs of chunk i+1.
+//  - Epilogue: 4 warps; thread t owns TMEM lane t = one hidden vector and
+//    reads its 128 scores with tcgen05.ld, keeping a sorted top-k_tile list
+//    of (score, position) in registers. A tile boundary flushes the list:
+//    ids are written through token_ids (ties: smaller vocabulary id).
+//  - A tile cut by a CTA boundary leaves partial lists in the workspace; the
+//    last CTA to finish a part (atomic ticket, no waiting) merges them.
+//  - Every mbarrier wait is bounded; on timeout the CTA raises an abort flag,
+//    records LMHEAD_ERR_TIMEOUT in the device error word, drains its own TMA
+//    copies, frees TMEM and exits.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_util.cuh"
+
+namespace lmhead {
+namespace {
+
+constexpr int kChunk = 128;                 // vocabulary rows per chunk (MMA N)
+constexpr int kHid = 128;                   // hidden vectors per CTA (MMA M, TMEM lanes)
+constexpr int kKBlock = 64;                 // bf16 per 128-byte swizzled row
+constexpr int kStageBytes = kChunk * 128;   // one 128-row x 64-element box
+constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kMaxStages = 12;
+constexpr int kTmemCols = 256;              // two 128-column fp32 accumulators
+constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kHid, kChunk);
+
+struct SharedCtl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t ufull;
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint32_t tmem_base;
+  int abort;
+  int decision[2];
+};
+
+struct Params {
+  const int32_t* token_ids;
+  int64_t n;
+  int r, M, T, k_tile, K;
+  int64_t n_chunks, tiles;
+  int G, stages;
+  int32_t* out_ids;
+  float* out_scores;
+  float2* partials;   // [HC][G][2][kHid][KT]
+  int* tile_tickets;  // [HC][tiles]
+  int* err;
+};
+
+__device__ __forceinline__ int32_t vocab_id(const Params& p, int64_t pos) {
+  if (pos >= p.n) return 0x7FFFFFFF;
+  return p.token_ids ? __ldg(p.token_ids + pos) : (int32_t)pos;
+}
+
+// Sorted (descending) top-KT list of (score, key); key is a position (ties
+// resolved through token_ids) or, for merged partials, a vocabulary id.
+template <int KT>
+struct TopK {
+  float s[KT];
+  int32_t k[KT];
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < KT; ++i) { s[i] = -INFINITY; k[i] = 0x7FFFFFFF; }
+  }
+  template <typename IdOf>
+  __device__ __forceinline__ static bool beats(float v, int32_t kv, float w, int32_t kw,
+                                               IdOf id_of) {
+    return v > w || (v == w && id_of(kv) < id_of(kw));
+  }
+  template <typename IdOf>
+  __device__ __forceinline__ void consider(float v, int32_t key, IdOf id_of) {
+    if (!(v >= s[KT - 1])) return;             // fast reject (also rejects NaN)
+    if (!beats(v, key, s[KT - 1], k[KT - 1], id_of)) return;
+    float cs = v;
+    int32_t ck = key;
+#pragma unroll
+    for (int i = 0; i < KT; ++i) {
+      if (beats(cs, ck, s[i], k[i], id_of)) {
+        const float ts = s[i]; s[i] = cs; cs = ts;
+        const int32_t tk = k[i]; k[i] = ck; ck = tk;
+      }
+    }
+  }
+};
+
+__device__ __forceinline__ int64_t chunk_start(int64_t b, int64_t nc, int G) { return b * nc / G; }
+// CTA owning chunk c under the balanced split start(b) = floor(b * nc / G).
+__device__ __forceinline__ int64_t cta_of_chunk(int64_t c, int64_t nc, int G) {
+  return ((c + 1) * G + nc - 1) / nc - 1;
+}
+
+template <int KT>
+__device__ __forceinline__ void write_tile(const Params& p, int m, int64_t tile, int count,
+                                           const TopK<KT>& L, bool keys_are_positions) {
+  int32_t* ids = p.out_ids + (size_t)m * p.K + (size_t)tile * KT;
+  float* sc = p.out_scores ? p.out_scores + (size_t)m * p.K + (size_t)tile * KT : nullptr;
+#pragma unroll
+  for (int j = 0; j < KT; ++j) {
+    if (j < count) {
+      ids[j] = keys_are_positions ? vocab_id(p, L.k[j]) : L.k[j];
+      if (sc) sc[j] = L.s[j];
+    }
+  }
+}
+
+template <int KT>
+__global__ void __launch_bounds__(kThreads, 1)
+local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
+                     const __grid_constant__ CUtensorMap umap, const Params p) {
+  extern __shared__ uint8_t dsmem_raw[];
+  __shared__ SharedCtl ctl;
+  uint8_t* dsmem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int kblocks = (p.r + kKBlock - 1) / kKBlock;
+  uint8_t* u_s = dsmem;
+  uint8_t* stage_s = dsmem + (size_t)kblocks * kStageBytes;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x, y = blockIdx.y;
+  const int64_t c0 = chunk_start(b, p.n_chunks, p.G);
+  const int64_t c1 = chunk_start(b + 1, p.n_chunks, p.G);
+  const int nch = (int)(c1 - c0);
+  const int NS = p.stages;
+  volatile int* abort_flag = &ctl.abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      tc::mbar_init(&ctl.full[s], 1);
+      tc::mbar_init(&ctl.empty[s], 1);
+    }
+    tc::mbar_init(&ctl.ufull, 1);
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&ctl.acc_full[a], 1);
+      tc::mbar_init(&ctl.acc_empty[a], 4);
+    }
+    ctl.abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&ctl.tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&amap);
+      tc::prefetch_tmap(&umap);
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // u comes from the previous kernel
+      tc::mbar_arrive_expect_tx(&ctl.ufull, (uint32_t)(kblocks * kStageBytes));
+      for (int kb = 0; kb < kblocks; ++kb)
+        tc::tma_load_2d(u_s + (size_t)kb * kStageBytes, &umap, &ctl.ufull, kb * kKBlock, y * kHid);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int i = 0; i < nch && ok; ++i) {
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = (int)(it % NS);
+          if (!tc::mbar_wait(&ctl.empty[s], ((it / NS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          tc::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
+          tc::tma_load_2d(stage_s + (size_t)s * kStageBytes, &amap, &ctl.full[s], kb * kKBlock,
+                          (int)((c0 + i) * kChunk));
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, kDevErrTimeout);
+      }
+      if (*abort_flag) {
+        // drain: wait (bounded) for the copies this thread issued last on every stage
+        const uint32_t first = it > (uint32_t)NS ? it - NS : 0;
+        for (uint32_t j = first; j < it; ++j) {
+          const long long t0 = clock64();
+          while (!tc::mbar_try_wait(&ctl.full[j % NS], (j / NS) & 1) &&
+                 clock64() - t0 < tc::kWaitCycles) {
+          }
+        }
+        const long long t0 = clock64();
+        while (!tc::mbar_try_wait(&ctl.ufull, 0) && clock64() - t0 < tc::kWaitCycles) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = tc::mbar_wait(&ctl.ufull, 0, abort_flag);
+      uint32_t it = 0;
+      for (int i = 0; i < nch && ok; ++i) {
+        const int a = i & 1;
+        if (!tc::mbar_wait(&ctl.acc_empty[a], ((i >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t d = tmem + a * kChunk;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = (int)(it % NS);
+          if (!tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint64_t adesc = tc::sw128_kmajor_desc(tc::smem_addr(u_s + (size_t)kb * kStageBytes));
+          const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_addr(stage_s + (size_t)s * kStageBytes));
+          const int nk = min(4, (p.r - kb * kKBlock + 15) / 16);
+          for (int k = 0; k < nk; ++k)
+            tc::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, (kb | k) != 0);
+          tc::mma_commit(&ctl.empty[s]);
+        }
+        if (!ok) break;
+        tc::mma_commit(&ctl.acc_full[a]);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, kDevErrTimeout);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int q = warp & 3;  // TMEM lane quadrant this warp may read
+    const int ml = q * 32 + lane;
+    const int m = y * kHid + ml;
+    const bool valid = m < p.M;
+    const int64_t n = p.n, T = p.T;
+    const int64_t P0 = c0 * kChunk;
+    const int64_t P1 = min(n, c1 * kChunk);
+    int64_t tile = P0 / T;
+    int64_t tile_end = min(n, tile * T + T);
+    const int64_t first_tile = tile;
+    const bool first_partial = P0 > tile * T;
+    auto id_of = [&](int32_t pos) { return vocab_id(p, pos); };
+    TopK<KT> cur, first, pend;
+    cur.reset();
+    first.reset();
+    bool have_first = false;
+    bool ok = true;
+    for (int i = 0; i < nch; ++i) {
+      const int a = i & 1;
+      int okw = 1;
+      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (i >> 1) & 1, abort_flag) ? 1 : 0;
+      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+      if (!okw) { ok = false; break; }
+      tc::fence_after_sync();
+      const int64_t cbase = (c0 + i) * kChunk;
+      for (int j0 = 0; j0 < kChunk; j0 += 32) {
+        if (cbase + j0 >= P1) break;
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kChunk + j0), v);
+        tc::tmem_ld_wait();
+        const int lim = (int)min((int64_t)32, P1 - (cbase + j0));
+        bool have_pend = false;
+        int64_t pend_tile = 0;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          if (jj < lim) {
+            const int64_t pos = cbase + j0 + jj;
+            if (pos == tile_end) {  // at most one boundary per 32 columns (T >= 32)
+              pend = cur;
+              have_pend = true;
+              pend_tile = tile;
+              cur.reset();
+              ++tile;
+              tile_end = min(n, tile_end + T);
+            }
+            cur.consider(__uint_as_float(v[jj]), (int32_t)pos, id_of);
+          }
+        }
+        if (have_pend) {
+          if (pend_tile == first_tile && first_partial) {
+            first = pend;
+            have_first = true;
+          } else if (valid) {
+            write_tile<KT>(p, m, pend_tile, (int)min((int64_t)KT, min(n, pend_tile * T + T) - pend_tile * T),
+                           pend, true);
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&ctl.acc_empty[a]);
+    }
+
+    // ---- tiles cut by CTA boundaries: publish parts, last part merges
+    const bool last_partial = (P1 < tile_end) || (tile == first_tile && first_partial);
+    const int tile_count_last = (int)min((int64_t)KT, tile_end - tile * T);
+    if (ok && valid && !last_partial) write_tile<KT>(p, m, tile, tile_count_last, cur, true);
+    // slot of this CTA's part of tile t: side 0 for its first tile, 1 for its last
+    int64_t part_tile[2] = {-1, -1};
+    if (have_first) part_tile[0] = first_tile;
+    if (last_partial) {
+      if (tile == first_tile) part_tile[0] = tile;
+      else part_tile[1] = tile;
+    }
+    if (ok && valid) {
+      for (int side = 0; side < 2; ++side) {
+        if (part_tile[side] < 0) continue;
+        const TopK<KT>& src = (side == 0 && have_first) ? first : cur;
+        float2* slot = p.partials + ((((size_t)y * p.G + b) * 2 + side) * kHid + ml) * KT;
+#pragma unroll
+        for (int j = 0; j < KT; ++j)
+          slot[j] = make_float2(src.s[j], __int_as_float(vocab_id(p, src.k[j])));
+      }
+    }
+    __threadfence();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (warp == 2 && lane == 0) {
+      const bool go = !(*abort_flag);
+      for (int side = 0; side < 2; ++side) {
+        ctl.decision[side] = 0;
+        const int64_t t = part_tile[side];
+        if (!go || t < 0) continue;
+        const int64_t fc = t * T / kChunk;
+        const int64_t lc = (min(n, t * T + T) - 1) / kChunk;
+        const int parts = (int)(cta_of_chunk(lc, p.n_chunks, p.G) - cta_of_chunk(fc, p.n_chunks, p.G) + 1);
+        __threadfence();
+        const int old = atomicAdd(p.tile_tickets + (size_t)y * p.tiles + t, 1);
+        ctl.decision[side] = (old == parts - 1) ? 1 : 0;
+      }
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    for (int side = 0; side < 2; ++side) {
+      if (!ctl.decision[side]) continue;
+      const int64_t t = part_tile[side];
+      __threadfence();
+      if (valid) {
+        const int64_t fc = t * T / kChunk;
+        const int64_t lc = (min(n, t * T + T) - 1) / kChunk;
+        const int64_t b0 = cta_of_chunk(fc, p.n_chunks, p.G), b1 = cta_of_chunk(lc, p.n_chunks, p.G);
+        TopK<KT> mg;
+        mg.reset();
+        auto same = [](int32_t id) { return id; };
+        for (int64_t bb = b0; bb <= b1; ++bb) {
+          const int64_t ft = chunk_start(bb, p.n_chunks, p.G) * kChunk / T;
+          const int sd = (t == ft) ? 0 : 1;
+          const float2* slot = p.partials + ((((size_t)y * p.G + bb) * 2 + sd) * kHid + ml) * KT;
+#pragma unroll
+          for (int j = 0; j < KT; ++j) {
+            const float2 e = __ldcg(slot + j);
+            mg.consider(e.x, __float_as_int(e.y), same);
+          }
+        }
+        write_tile<KT>(p, m, t, (int)min((int64_t)KT, min(n, t * T + T) - t * T), mg, false);
+      }
+      if (warp == 2 && lane == 0) p.tile_tickets[(size_t)y * p.tiles + t] = 0;
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      if (lane == 0) record_error(p.err, kDevErrTimeout);
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// rows x cols bf16 row-major; box = 128 rows x 64 columns, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {kKBlock, kChunk};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!cache[dev]) cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
+  return cache[dev];
+}
+
+template <int KT>
+cudaError_t launch_kt(const CUtensorMap& amap, const CUtensorMap& umap, const Params& p, int HC,
+                      size_t smem, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(local_topk_tc_kernel<KT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  local_topk_tc_kernel<KT><<<dim3(p.G, HC), kThreads, smem, s>>>(amap, umap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool local_topk_tc_supported(int r, int T, int k_tile) {
+  return r <= kLocalTcMaxR && T >= 32 &&
+         (k_tile == 1 || k_tile == 2 || k_tile == 4 || k_tile == 8);
+}
+
+size_t local_topk_tc_scratch_bytes(int64_t n, int M, int T) {
+  const int64_t HC = (M + kHid - 1) / kHid;
+  const int64_t tiles = (n + T - 1) / T;
+  (void)tiles;
+  return (size_t)HC * kLocalTcMaxCtas * 2 * kHid * 8 * sizeof(float2);
+}
+
+int local_topk_tc_tickets(int64_t n, int M, int T) {
+  const int64_t HC = (M + kHid - 1) / kHid;
+  return (int)(HC * ((n + T - 1) / T));
+}
+
+cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
+                                 int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,
+                                 float* out_scores, void* partials, int* tile_tickets, int* err,
+                                 cudaStream_t s) {
+  Params p;
+  p.token_ids = token_ids;
+  p.n = n;
+  p.r = r;
+  p.M = M;
+  p.T = T;
+  p.k_tile = k_tile;
+  const int64_t full = n / T, tail = n - full * T;
+  p.K = (int)(full * k_tile + (tail ? (tail < k_tile ? tail : k_tile) : 0));
+  p.n_chunks = (n + kChunk - 1) / kChunk;
+  p.tiles = (n + T - 1) / T;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  p.G = (int)min((int64_t)min(sms, kLocalTcMaxCtas), p.n_chunks);
+  const int kblocks = (r + kKBlock - 1) / kKBlock;
+  const size_t u_bytes = (size_t)kblocks * kStageBytes;
+  const size_t budget = 232448 - 2048;  // opt-in shared memory minus static + alignment slack
+  int stages = (int)((budget - 1024 - u_bytes) / kStageBytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return cudaErrorInvalidValue;
+  p.stages = stages;
+  p.out_ids = out_ids;
+  p.out_scores = out_scores;
+  p.partials = static_cast<float2*>(partials);
+  p.tile_tickets = tile_tickets;
+  p.err = err;
+  CUtensorMap amap, umap;
+  if (!make_map(&amap, A, (uint64_t)n, (uint64_t)r) || !make_map(&umap, u, (uint64_t)M, (uint64_t)r))
+    return cudaErrorInvalidValue;
+  const int HC = (M + kHid - 1) / kHid;
+  const size_t smem = 1024 + u_bytes + (size_t)stages * kStageBytes;
+  switch (k_tile) {
+    case 1: return launch_kt<1>(amap, umap, p, HC, smem, s);
+    case 2: return launch_kt<2>(amap, umap, p, HC, smem, s);
+    case 4: return launch_kt<4>(amap, umap, p, HC, smem, s);
+    case 8: return launch_kt<8>(amap, umap, p, HC, smem, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace lmhead
