@@ -163,7 +163,24 @@ def oracle_sample_rate(head, h_bits, budget_s=12.0, rows=4):
 
 
 # ---------------------------------------------------------------- GPU arm
+def make_graph(torch, fn):
+    """Capture fn() (a sequence of library calls on the current stream)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
 def run_ours(args):
+    import ctypes
+
     import torch
     import torch.distributed as dist
 
@@ -179,10 +196,10 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     import draft_lm_head_gb300 as L
-    L.load()
+    lib = L.load()
 
     wl = WORKLOAD
-    M = args.M
+    n, d, r, M = wl.n, wl.d, wl.r, args.M
     head = head_inputs()
     hb = hidden(head["W"], M, rank)
 
@@ -194,20 +211,34 @@ def run_ours(args):
     h0 = dev(hb)
     rot = [(W0, A0, B0, tok0, h0)] + [(W0.clone(), A0.clone(), B0.clone(), tok0.clone(), h0.clone())
                                       for _ in range(NROT - 1)]
-    K = L.candidate_count(L.LOCAL, wl.n, wl.T, wl.k_tile)
+    K = L.candidate_count(L.LOCAL, n, wl.T, wl.k_tile)
+    nl = lib.lmhead_two_stage_launches(L.LOCAL, wl.k_tile)
     ws = L.Workspace()
-    outs = [(torch.empty((M, K), dtype=torch.int32, device="cuda"),
-             torch.empty((M, K), dtype=torch.float32, device="cuda"),
-             torch.empty((M, K), dtype=torch.float32, device="cuda")) for _ in range(NROT)]
 
-    def step(i, Mx=M, hx=None):
-        Wt, At, Bt, tk, ht = rot[i % NROT]
-        return L.two_stage(L.LOCAL, Wt, At, Bt, ht if hx is None else hx, tk, wl.T, wl.k_tile,
-                           workspace=ws, out=outs[i % NROT] if Mx == M else None)
+    def outputs(Mx):
+        return [(torch.empty((Mx, K), dtype=torch.int32, device="cuda"),
+                 torch.empty((Mx, K), dtype=torch.float32, device="cuda"),
+                 torch.empty((Mx, K), dtype=torch.float32, device="cuda")) for _ in range(NROT)]
+
+    outs = outputs(M)
+
+    def step(j, hx=None, out=None):
+        Wt, At, Bt, tk, ht = rot[j % NROT]
+        return L.two_stage(L.LOCAL, Wt, At, Bt, ht if hx is None else hx[j % NROT], tk, wl.T,
+                           wl.k_tile, workspace=ws, out=(out or outs)[j % NROT])
+
+    # one graph holding NROT consecutive steps (one per input copy), plus singles
+    g_all = make_graph(torch, lambda: [step(j) for j in range(NROT)])
+    g_one = [make_graph(torch, lambda j=j: step(j)) for j in range(NROT)]
+
+    def run_steps(k):
+        for _ in range(k // NROT):
+            g_all.replay()
+        for j in range(k % NROT):
+            g_one[j].replay()
 
     sampler = ClockSampler(local)
-    for i in range(max(args.warmup, 3)):
-        step(i)
+    run_steps(max(args.warmup, 3))
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
@@ -216,8 +247,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(args.steps):
-        step(i)
+    run_steps(args.steps)
     e1.record()
     torch.cuda.synchronize()
     if world > 1:
@@ -228,36 +258,39 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     value = world * M * args.steps / (ms / 1e3)
-    launches = L.load().lmhead_two_stage_launches(L.LOCAL, wl.k_tile) * args.steps
+    launches = nl * args.steps
 
-    # per-kernel durations over the same number of steps (events between launches)
-    nl = L.load().lmhead_two_stage_launches(L.LOCAL, wl.k_tile)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
+    # per-kernel durations: the profiled entry point records an event after every launch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(NROT)]
     for row in evs:
         for e in row:
             e.record()
     torch.cuda.synchronize()
-    import ctypes
-    lib = L.load()
-    stream = torch.cuda.current_stream().cuda_stream
-    for i in range(args.steps):
-        Wt, At, Bt, tk, ht = rot[i % NROT]
-        ids, lg, q = outs[i % NROT]
-        handles = (ctypes.c_void_p * (nl + 1))(*[e.cuda_event for e in evs[i]])
-        buf = ws.get(L.workspace_size(L.LOCAL, wl.n, wl.d, wl.r, M, wl.T, wl.k_tile), ids.device)
+    wsb = ws.get(L.workspace_size(L.LOCAL, n, d, r, M, wl.T, wl.k_tile), h0.device)
+
+    def prof_step(j):
+        Wt, At, Bt, tk, ht = rot[j]
+        ids, lg, q = outs[j]
+        handles = (ctypes.c_void_p * (nl + 1))(*[e.cuda_event for e in evs[j]])
         L.check(lib.lmhead_two_stage_profiled(
             L.LOCAL, Wt.data_ptr(), At.data_ptr(), Bt.data_ptr(), ht.data_ptr(), tk.data_ptr(),
-            wl.n, wl.d, wl.r, M, wl.T, wl.k_tile, 1.0, ids.data_ptr(), lg.data_ptr(), q.data_ptr(),
-            buf.data_ptr(), buf.numel(), handles, nl + 1, stream), "two_stage_profiled")
-    torch.cuda.synchronize()
-    names = ["project_u", "score_local_topk", "gather_logits_softmax"]
-    kern_us = {names[k]: 1e3 * statistics.fmean(evs[i][k].elapsed_time(evs[i][k + 1])
-                                                 for i in range(args.steps)) for k in range(nl)}
+            n, d, r, M, wl.T, wl.k_tile, 1.0, ids.data_ptr(), lg.data_ptr(), q.data_ptr(),
+            wsb.data_ptr(), wsb.numel(), handles, nl + 1,
+            torch.cuda.current_stream().cuda_stream), "two_stage_profiled")
 
-    # unique gathered rows -> algorithmic bytes
+    names = ["project_u", "score_local_topk", "gather_logits_softmax"][:nl]
+    samples = {k: [] for k in names}
+    prof_mode = "stream, events between the launches of one call"
+    for i in range(args.steps):
+        j = i % NROT
+        prof_step(j)
+        torch.cuda.synchronize()
+        for k, nm in enumerate(names):
+            samples[nm].append(evs[j][k].elapsed_time(evs[j][k + 1]))
+    kern_us = {k: 1e3 * statistics.fmean(v) for k, v in samples.items()}
+
     ids_h = outs[0][0].cpu().numpy()
     U = int(np.unique(ids_h).size)
-    n, d, r = wl.n, wl.d, wl.r
     bytes_kernel = {
         "project_u": 2 * r * d + 2 * M * d + 2 * M * r,
         "score_local_topk": 2 * n * r + 2 * M * r + 4 * M * K,
@@ -269,9 +302,9 @@ def run_ours(args):
     achieved = bytes_kernel[dom] / (kern_us[dom] * 1e-6) / 1e9
     roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
             "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
-            "bytes_per_launch": bytes_kernel[dom], "traffic": None}
+            "bytes_per_launch": bytes_kernel[dom], "traffic": None, "timing": prof_mode}
 
-    # end to end through the public API, host buffers, copies inside the timed region
+    # end to end through the public API: host buffers, copies inside the timed region
     h_host = [torch.from_numpy(np.ascontiguousarray(hb).view(np.int16)).view(torch.bfloat16).pin_memory()
               for _ in range(NROT)]
     host_out = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[0])
@@ -304,40 +337,40 @@ def run_ours(args):
            "h2d_bytes_per_step": int(hb.nbytes),
            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs[0]))}
 
-    # sweep over M and the dense head, for context
+    # sweep over M (graph replay) with the dense head beside it, for context
     sweep = []
     if not args.no_sweep and rank == 0:
+        reps = 40
         for Mx in (1, 8, 16, 32, 64):
-            hx_bits = hidden(head["W"], Mx, rank)
-            hx = dev(hx_bits)
-            reps = 30
-            for i in range(3):
-                step(i, Mx, hx)
+            hxs = [dev(hidden(head["W"], Mx, rank)) for _ in range(NROT)]
+            ox = outputs(Mx)
+            g = make_graph(torch, lambda: [step(j, hxs, ox) for j in range(NROT)])
+            g.replay()
             torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            for i in range(reps):
-                res = step(i, Mx, hx)
+            for _ in range(reps // NROT):
+                g.replay()
             b.record()
             torch.cuda.synchronize()
-            us = a.elapsed_time(b) * 1e3 / reps
-            Ux = int(np.unique(res[0].cpu().numpy()).size)
+            us = a.elapsed_time(b) * 1e3 / (reps // NROT * NROT)
+            Ux = int(np.unique(ox[0][0].cpu().numpy()).size)
             by = 2 * n * r + 2 * r * d + 2 * Mx * d + 2 * d * Ux + 12 * Mx * K
             dl = torch.empty((Mx, n), dtype=torch.float32, device="cuda")
             dq = torch.empty((Mx, n), dtype=torch.float32, device="cuda")
-            for i in range(2):
-                L.dense_head(rot[i % NROT][0], hx, out=(dl, dq))
-            torch.cuda.synchronize()
+            gd = make_graph(torch, lambda: [L.dense_head(rot[j][0], hxs[j], out=(dl, dq))
+                                            for j in range(2)])
             a.record()
-            for i in range(reps):
-                L.dense_head(rot[i % NROT][0], hx, out=(dl, dq))
+            for _ in range(4):
+                gd.replay()
             b.record()
             torch.cuda.synchronize()
-            dus = a.elapsed_time(b) * 1e3 / reps
+            dus = a.elapsed_time(b) * 1e3 / 8
             sweep.append({"M": Mx, "us": round(us, 2), "vecs_per_s": round(Mx / us * 1e6, 1),
                           "unique_rows": Ux, "bytes": by,
                           "hbm_frac": round(by / (us * 1e-6) / 1e9 / hbm, 4),
                           "dense_us": round(dus, 2)})
+            del g, gd
     clocks = sampler.stop()
 
     cpu = None
@@ -357,6 +390,7 @@ def run_ours(args):
                        "n": n, "d": d, "r": r, "M": M, "mode": "local", "tile": wl.T,
                        "k_tile": wl.k_tile, "candidates": K,
                        "l2": f"{NROT} rotating copies of every input (> 2x L2)",
+                       "launch": "CUDA graph replay of library calls",
                        "parallelism": f"replicas x{world} (independent hidden vectors)"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks, "kernel_us": {k: round(v, 3) for k, v in kern_us.items()},

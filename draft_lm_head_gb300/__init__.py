@@ -13,6 +13,7 @@ draft_lm_head_gb300.prep.
 """
 from __future__ import annotations
 
+import functools
 from typing import Optional
 
 import torch
@@ -56,6 +57,7 @@ def version() -> int:
     return load().lmhead_version()
 
 
+@functools.lru_cache(maxsize=4096)
 def candidate_count(mode: int, n: int, C_or_tile: int, k_tile: int = 0) -> int:
     K = load().lmhead_candidate_count(mode, n, C_or_tile, k_tile)
     if K < 0:
@@ -63,6 +65,7 @@ def candidate_count(mode: int, n: int, C_or_tile: int, k_tile: int = 0) -> int:
     return int(K)
 
 
+@functools.lru_cache(maxsize=4096)
 def workspace_size(mode: int, n: int, d: int, r: int, M: int, C_or_tile: int,
                    k_tile: int = 0) -> int:
     return int(load().lmhead_workspace_size(mode, n, d, r, M, C_or_tile, k_tile))

@@ -103,7 +103,14 @@ struct Marks {
   int next = 0;
   cudaError_t mark(cudaStream_t s) {
     if (next < n && events && events[next]) {
-      cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[next]), s);
+      // inside a stream capture the record must be external to stay observable
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      cudaError_t e = cudaStreamIsCapturing(s, &cs);
+      if (e != cudaSuccess) return e;
+      e = cs == cudaStreamCaptureStatusActive
+              ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[next]), s,
+                                         cudaEventRecordExternal)
+              : cudaEventRecord(static_cast<cudaEvent_t>(events[next]), s);
       ++next;
       return e;
     }

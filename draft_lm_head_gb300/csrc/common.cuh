@@ -91,4 +91,18 @@ __device__ __forceinline__ bool beats(float sa, int32_t ia, float sb, int32_t ib
   return sa > sb || (sa == sb && ia < ib);
 }
 
+// Raise a kernel's dynamic shared-memory limit, once per device and size:
+// the attribute call is slow enough to starve the GPU if made per launch.
+template <typename Kernel>
+inline cudaError_t ensure_dynamic_smem(Kernel kernel, size_t bytes, int* cache64) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if ((size_t)cache64[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cache64[dev] = (int)bytes;
+  return e;
+}
+
 }  // namespace lmhead

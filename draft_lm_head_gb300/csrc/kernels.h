@@ -2,6 +2,7 @@
 // cudaError_t from the launch; arguments have been validated by api.cu.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -14,8 +15,10 @@ constexpr int kFusedMaxKTile = 32;
 // Largest selection budget of the radix select (global C or k_tile).
 constexpr int kSelectMaxK = 4096;
 
-// K1: u = bf16(B h), fp32 accumulation. Also zeroes `zero_ints` ints at
+// K1: u = bf16(B h), fp32 accumulation. Tensor cores (cluster split over d)
+// up to d = kProjTcMaxD, CUDA cores beyond. Also zeroes `zero_ints` ints at
 // `zero_ptr` (tickets of the fused kernels that follow), if non-null.
+constexpr int kProjTcMaxD = 5120;
 cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int M, bf16_t* u,
                              int* zero_ptr, int zero_ints, cudaStream_t s);
 
@@ -61,5 +64,11 @@ cudaError_t launch_dense_logits(const bf16_t* W, const bf16_t* h, int64_t n, int
                                 float* logits, cudaStream_t s);
 
 int* device_error_word();  // this device's error word (nullptr on failure)
+
+// TMA map of a rows x cols bf16 row-major matrix: box_rows x box_cols
+// (box_cols * 2 == 128 bytes), 128-byte swizzle, zero fill out of bounds.
+bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows, uint32_t box_cols);
+int sm_count();  // SMs of the current device (cached)
 
 }  // namespace lmhead

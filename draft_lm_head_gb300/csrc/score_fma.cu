@@ -182,8 +182,8 @@ cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_
   const int K = (int)(full * k_tile + (tail ? (tail < k_tile ? tail : k_tile) : 0));
   const size_t smem = (size_t)kMB * r * sizeof(float);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(local_topk_fma_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static int smem_set[64] = {0};
+    cudaError_t e = ensure_dynamic_smem(local_topk_fma_kernel, smem, smem_set);
     if (e != cudaSuccess) return e;
   }
   dim3 grid((unsigned)tiles, (M + kMB - 1) / kMB);
@@ -196,8 +196,8 @@ cudaError_t launch_score_all_fma(const bf16_t* A, const bf16_t* u, int64_t n, in
                                  float* S, cudaStream_t s) {
   const size_t smem = (size_t)kMB * r * sizeof(float);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(score_all_fma_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static int smem_set[64] = {0};
+    cudaError_t e = ensure_dynamic_smem(score_all_fma_kernel, smem, smem_set);
     if (e != cudaSuccess) return e;
   }
   dim3 grid((unsigned)((n + kChunk - 1) / kChunk), (M + kMB - 1) / kMB);

@@ -57,6 +57,7 @@ struct Params {
   int r, M, T, k_tile, K;
   int64_t n_chunks, tiles;
   int G, stages;
+  int lane_shift;  // 64 when M <= 64: hidden rows sit in TMEM lanes 64..127
   int32_t* out_ids;
   float* out_scores;
   float2* partials;   // [HC][G][2][kHid][KT]
@@ -69,30 +70,65 @@ __device__ __forceinline__ int32_t vocab_id(const Params& p, int64_t pos) {
   return p.token_ids ? __ldg(p.token_ids + pos) : (int32_t)pos;
 }
 
-// Sorted (descending) top-KT list of (score, key); key is a position (ties
-// resolved through token_ids) or, for merged partials, a vocabulary id.
-template <int KT>
-struct TopK {
+// Sorted (descending) top-KT list of (score, key), kept in registers. The key
+// is a position (ties resolved through token_ids) or, for merged partials, a
+// vocabulary id. push() is branch-free for distinct scores: every column of
+// every lane runs the same few compares and selects (32 independent lanes
+// would otherwise diverge on almost every column). A NaN score is a no-op.
+// Only an exact tie with a listed score takes the branch that compares
+// vocabulary ids.
+template <int KT, bool kPositions>
+struct RegList {
   float s[KT];
   int32_t k[KT];
+
   __device__ __forceinline__ void reset() {
 #pragma unroll
     for (int i = 0; i < KT; ++i) { s[i] = -INFINITY; k[i] = 0x7FFFFFFF; }
   }
-  template <typename IdOf>
-  __device__ __forceinline__ static bool beats(float v, int32_t kv, float w, int32_t kw,
-                                               IdOf id_of) {
-    return v > w || (v == w && id_of(kv) < id_of(kw));
+
+  __device__ __forceinline__ static int32_t vocab(int32_t key, const int32_t* tok, int64_t n) {
+    if (!kPositions) return key;
+    if (key >= n) return 0x7FFFFFFF;
+    return tok ? __ldg(tok + key) : key;
   }
-  template <typename IdOf>
-  __device__ __forceinline__ void consider(float v, int32_t key, IdOf id_of) {
-    if (!(v >= s[KT - 1])) return;             // fast reject (also rejects NaN)
-    if (!beats(v, key, s[KT - 1], k[KT - 1], id_of)) return;
-    float cs = v;
+
+  // Branch-free insertion by strict score order. A score equal to a listed
+  // one is not inserted; push_fast returns true and the caller inserts it
+  // later with push_exact.
+  __device__ __forceinline__ bool push_fast(float x, int32_t key) {
+    bool tie = false;
+#pragma unroll
+    for (int i = 0; i < KT; ++i) tie |= (x == s[i]);
+    const float xe = tie ? __int_as_float(0x7FC00000) : x;
+    bool c[KT];
+#pragma unroll
+    for (int i = 0; i < KT; ++i) c[i] = xe > s[i];
+#pragma unroll
+    for (int i = KT - 1; i > 0; --i) {
+      s[i] = c[i] ? (c[i - 1] ? s[i - 1] : xe) : s[i];
+      k[i] = c[i] ? (c[i - 1] ? k[i - 1] : key) : k[i];
+    }
+    s[0] = c[0] ? xe : s[0];
+    k[0] = c[0] ? key : k[0];
+    return tie;
+  }
+
+  // Merge another list into this one (exact order).
+  __device__ __forceinline__ void absorb(const RegList& o, const int32_t* tok, int64_t n) {
+#pragma unroll
+    for (int i = 0; i < KT; ++i)
+      push_exact(o.s[i] == -INFINITY ? __int_as_float(0x7FC00000) : o.s[i], o.k[i], tok, n);
+  }
+
+  // Exact insertion: score descending, then the smaller vocabulary id.
+  __device__ __forceinline__ void push_exact(float x, int32_t key, const int32_t* tok, int64_t n) {
+    float cs = x;
     int32_t ck = key;
 #pragma unroll
     for (int i = 0; i < KT; ++i) {
-      if (beats(cs, ck, s[i], k[i], id_of)) {
+      const bool wins = cs > s[i] || (cs == s[i] && vocab(ck, tok, n) < vocab(k[i], tok, n));
+      if (wins) {
         const float ts = s[i]; s[i] = cs; cs = ts;
         const int32_t tk = k[i]; k[i] = ck; ck = tk;
       }
@@ -106,9 +142,9 @@ __device__ __forceinline__ int64_t cta_of_chunk(int64_t c, int64_t nc, int G) {
   return ((c + 1) * G + nc - 1) / nc - 1;
 }
 
-template <int KT>
+template <int KT, bool kPos>
 __device__ __forceinline__ void write_tile(const Params& p, int m, int64_t tile, int count,
-                                           const TopK<KT>& L, bool keys_are_positions) {
+                                           const RegList<KT, kPos>& L, bool keys_are_positions) {
   int32_t* ids = p.out_ids + (size_t)m * p.K + (size_t)tile * KT;
   float* sc = p.out_scores ? p.out_scores + (size_t)m * p.K + (size_t)tile * KT : nullptr;
 #pragma unroll
@@ -170,7 +206,8 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       asm volatile("griddepcontrol.wait;" ::: "memory");  // u comes from the previous kernel
       tc::mbar_arrive_expect_tx(&ctl.ufull, (uint32_t)(kblocks * kStageBytes));
       for (int kb = 0; kb < kblocks; ++kb)
-        tc::tma_load_2d(u_s + (size_t)kb * kStageBytes, &umap, &ctl.ufull, kb * kKBlock, y * kHid);
+        tc::tma_load_2d(u_s + (size_t)kb * kStageBytes, &umap, &ctl.ufull, kb * kKBlock,
+                        y * kHid - p.lane_shift);  // rows before 0 are zero-filled
       uint32_t it = 0;
       bool ok = true;
       for (int i = 0; i < nch && ok; ++i) {
@@ -234,8 +271,8 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int q = warp & 3;  // TMEM lane quadrant this warp may read
     const int ml = q * 32 + lane;
-    const int m = y * kHid + ml;
-    const bool valid = m < p.M;
+    const int m = y * kHid + ml - p.lane_shift;
+    const bool valid = m >= 0 && m < p.M;
     const int64_t n = p.n, T = p.T;
     const int64_t P0 = c0 * kChunk;
     const int64_t P1 = min(n, c1 * kChunk);
@@ -243,12 +280,24 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
     int64_t tile_end = min(n, tile * T + T);
     const int64_t first_tile = tile;
     const bool first_partial = P0 > tile * T;
-    auto id_of = [&](int32_t pos) { return vocab_id(p, pos); };
-    TopK<KT> cur, first, pend;
-    cur.reset();
+    const float kNaN = __int_as_float(0x7FC00000);  // a pushed NaN changes nothing
+    // kSub independent sub-lists (column jj goes to jj % kSub) break the
+    // serial dependency between consecutive columns; merged at tile ends
+    constexpr int kSub = KT <= 4 ? 4 : 2;
+    RegList<KT, true> sub[kSub], cur, first;
+#pragma unroll
+    for (int j = 0; j < kSub; ++j) sub[j].reset();
     first.reset();
-    bool have_first = false;
+    auto merged = [&]() {
+      RegList<KT, true> L = sub[0];
+#pragma unroll
+      for (int j = 1; j < kSub; ++j) L.absorb(sub[j], p.token_ids, n);
+      return L;
+    };
     bool ok = true;
+    // warps whose 32 hidden rows all lie outside [0, M) only pace the ring
+    const int m_lo = y * kHid + q * 32 - p.lane_shift;
+    const bool warp_live = m_lo + 31 >= 0 && m_lo < p.M;
     for (int i = 0; i < nch; ++i) {
       const int a = i & 1;
       int okw = 1;
@@ -257,36 +306,44 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       if (!okw) { ok = false; break; }
       tc::fence_after_sync();
       const int64_t cbase = (c0 + i) * kChunk;
-      for (int j0 = 0; j0 < kChunk; j0 += 32) {
-        if (cbase + j0 >= P1) break;
+      for (int j0 = 0; j0 < kChunk && warp_live; j0 += 32) {
+        const int64_t base = cbase + j0;
+        if (base >= P1) break;
         uint32_t v[32];
         tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kChunk + j0), v);
         tc::tmem_ld_wait();
-        const int lim = (int)min((int64_t)32, P1 - (cbase + j0));
-        bool have_pend = false;
-        int64_t pend_tile = 0;
+        const int lim = (int)min((int64_t)32, P1 - base);
+        // columns [0, bnd) belong to the current tile; at most one boundary
+        // falls inside 32 columns because T >= 32
+        const int bnd = (int)min((int64_t)lim, tile_end - base);
+        uint32_t ties = 0;  // columns held back by an exact tie
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
-          if (jj < lim) {
-            const int64_t pos = cbase + j0 + jj;
-            if (pos == tile_end) {  // at most one boundary per 32 columns (T >= 32)
-              pend = cur;
-              have_pend = true;
-              pend_tile = tile;
-              cur.reset();
-              ++tile;
-              tile_end = min(n, tile_end + T);
-            }
-            cur.consider(__uint_as_float(v[jj]), (int32_t)pos, id_of);
-          }
+          const bool t = sub[jj % kSub].push_fast(
+              jj < bnd && valid ? __uint_as_float(v[jj]) : kNaN, (int32_t)(base + jj));
+          ties |= (t ? 1u : 0u) << jj;
         }
-        if (have_pend) {
-          if (pend_tile == first_tile && first_partial) {
-            first = pend;
-            have_first = true;
-          } else if (valid) {
-            write_tile<KT>(p, m, pend_tile, (int)min((int64_t)KT, min(n, pend_tile * T + T) - pend_tile * T),
-                           pend, true);
+        if (ties != 0 || bnd < lim) {  // rare: a tie, or a tile ends inside this batch
+          float rest[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) rest[jj] = __uint_as_float(v[jj]);
+          for (uint32_t t = ties; t; t &= t - 1) {
+            const int jj = __ffs(t) - 1;
+            sub[0].push_exact(rest[jj], (int32_t)(base + jj), p.token_ids, n);
+          }
+          if (bnd < lim) {
+            cur = merged();
+            if (tile == first_tile && first_partial) {
+              first = cur;  // part of a tile cut by this CTA's start
+            } else if (valid) {
+              write_tile<KT>(p, m, tile, (int)min((int64_t)KT, tile_end - tile * T), cur, true);
+            }
+#pragma unroll
+            for (int j = 0; j < kSub; ++j) sub[j].reset();
+            ++tile;
+            tile_end = min(n, tile_end + T);
+            for (int jj = bnd; jj < lim; ++jj)
+              sub[0].push_exact(valid ? rest[jj] : kNaN, (int32_t)(base + jj), p.token_ids, n);
           }
         }
       }
@@ -294,22 +351,23 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&ctl.acc_empty[a]);
     }
+    cur = merged();
 
-    // ---- tiles cut by CTA boundaries: publish parts, last part merges
-    const bool last_partial = (P1 < tile_end) || (tile == first_tile && first_partial);
-    const int tile_count_last = (int)min((int64_t)KT, tile_end - tile * T);
-    if (ok && valid && !last_partial) write_tile<KT>(p, m, tile, tile_count_last, cur, true);
-    // slot of this CTA's part of tile t: side 0 for its first tile, 1 for its last
-    int64_t part_tile[2] = {-1, -1};
-    if (have_first) part_tile[0] = first_tile;
-    if (last_partial) {
-      if (tile == first_tile) part_tile[0] = tile;
-      else part_tile[1] = tile;
-    }
+    // ---- tiles cut by CTA boundaries: publish parts, last part merges.
+    // Which tiles are cut depends only on this CTA's range [P0, P1).
+    const int64_t last_tile = (P1 - 1) / T;
+    const int64_t last_end = min(n, last_tile * T + T);
+    const bool first_cut = P0 > first_tile * T || P1 < min(n, first_tile * T + T);
+    const bool last_cut = last_tile != first_tile && P1 < last_end;
+    int64_t part_tile[2] = {first_cut ? first_tile : -1, last_cut ? last_tile : -1};
+    // the running list now holds the last tile; complete unless cut
+    const bool last_is_cut = (last_tile == first_tile) ? first_cut : last_cut;
+    if (ok && valid && !last_is_cut)
+      write_tile<KT>(p, m, last_tile, (int)min((int64_t)KT, last_end - last_tile * T), cur, true);
     if (ok && valid) {
       for (int side = 0; side < 2; ++side) {
         if (part_tile[side] < 0) continue;
-        const TopK<KT>& src = (side == 0 && have_first) ? first : cur;
+        const RegList<KT, true>& src = (side == 0 && last_tile != first_tile) ? first : cur;
         float2* slot = p.partials + ((((size_t)y * p.G + b) * 2 + side) * kHid + ml) * KT;
 #pragma unroll
         for (int j = 0; j < KT; ++j)
@@ -341,9 +399,8 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
         const int64_t fc = t * T / kChunk;
         const int64_t lc = (min(n, t * T + T) - 1) / kChunk;
         const int64_t b0 = cta_of_chunk(fc, p.n_chunks, p.G), b1 = cta_of_chunk(lc, p.n_chunks, p.G);
-        TopK<KT> mg;
+        RegList<KT, false> mg;
         mg.reset();
-        auto same = [](int32_t id) { return id; };
         for (int64_t bb = b0; bb <= b1; ++bb) {
           const int64_t ft = chunk_start(bb, p.n_chunks, p.G) * kChunk / T;
           const int sd = (t == ft) ? 0 : 1;
@@ -351,7 +408,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
 #pragma unroll
           for (int j = 0; j < KT; ++j) {
             const float2 e = __ldcg(slot + j);
-            mg.consider(e.x, __float_as_int(e.y), same);
+            mg.push_exact(e.x == -INFINITY ? kNaN : e.x, __float_as_int(e.y), nullptr, n);
           }
         }
         write_tile<KT>(p, m, t, (int)min((int64_t)KT, min(n, t * T + T) - t * T), mg, false);
@@ -373,51 +430,11 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
 }
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
-
-// rows x cols bf16 row-major; box = 128 rows x 64 columns, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {kKBlock, kChunk};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int sm_count() {
-  static int cache[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (!cache[dev]) cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
-  return cache[dev];
-}
-
 template <int KT>
 cudaError_t launch_kt(const CUtensorMap& amap, const CUtensorMap& umap, const Params& p, int HC,
                       size_t smem, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(local_topk_tc_kernel<KT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static int smem_set[64] = {0};
+  cudaError_t e = ensure_dynamic_smem(local_topk_tc_kernel<KT>, smem, smem_set);
   if (e != cudaSuccess) return e;
   local_topk_tc_kernel<KT><<<dim3(p.G, HC), kThreads, smem, s>>>(amap, umap, p);
   return cudaGetLastError();
@@ -467,13 +484,15 @@ cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return cudaErrorInvalidValue;
   p.stages = stages;
+  p.lane_shift = M <= 64 ? 64 : 0;
   p.out_ids = out_ids;
   p.out_scores = out_scores;
   p.partials = static_cast<float2*>(partials);
   p.tile_tickets = tile_tickets;
   p.err = err;
   CUtensorMap amap, umap;
-  if (!make_map(&amap, A, (uint64_t)n, (uint64_t)r) || !make_map(&umap, u, (uint64_t)M, (uint64_t)r))
+  if (!make_bf16_map(&amap, A, (uint64_t)n, (uint64_t)r, kChunk, kKBlock) ||
+      !make_bf16_map(&umap, u, (uint64_t)M, (uint64_t)r, kHid, kKBlock))
     return cudaErrorInvalidValue;
   const int HC = (M + kHid - 1) / kHid;
   const size_t smem = 1024 + u_bytes + (size_t)stages * kStageBytes;

@@ -175,8 +175,8 @@ cudaError_t launch_segment_topk(const float* S, const int32_t* token_ids, int64_
   const int64_t full = n / seg_len, tail = n - full * seg_len;
   const int K = (int)(full * k + (tail ? (tail < k ? tail : k) : 0));
   const size_t smem = 2 * kCap * sizeof(uint64_t) + (kBins + kThreads) * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(segment_topk_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static int smem_set[64] = {0};
+  cudaError_t e = ensure_dynamic_smem(segment_topk_kernel, smem, smem_set);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)segs, M);
   segment_topk_kernel<<<grid, kThreads, smem, s>>>(S, token_ids, n, seg_len, k, K, out_ids,

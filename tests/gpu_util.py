@@ -79,10 +79,15 @@ def workload_case(wl, M, shuffle=None, tree=None, stream_offset=0):
             "h": h, "t": t, "counts": head["counts"], "n": wl.n, "d": wl.d, "r": wl.r, "M": M}
 
 
-def oracle_scores(case):
-    """Oracle u (bf16 grid, fp64) and position-ordered scores M x n."""
+def oracle_scores(case, with_slack=False):
+    """Oracle u (bf16 grid, fp64) and position-ordered scores M x n (and the
+    u-rounding slack of tests/parity.py when asked)."""
+    import parity
     A64 = O.bf16_bits_to_f64(case["A"])
     B64 = O.bf16_bits_to_f64(case["B"])
     h64 = O.bf16_bits_to_f64(case["h"])
     u = O.project_u(B64, h64)
-    return u, O.lowrank_scores(A64, u), h64
+    S = O.lowrank_scores(A64, u)
+    if with_slack:
+        return u, S, h64, parity.u_slack(A64, B64, h64)
+    return u, S, h64

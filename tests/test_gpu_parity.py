@@ -39,7 +39,7 @@ def _u_ok(gpu_u_bits, case):
     diff = got != ora
     if not diff.any():
         return 0
-    err_bound = case["d"] * 2.0 ** -23 * (np.abs(h64) @ np.abs(B64).T)
+    err_bound = P.U_GAMMA * (np.abs(h64) @ np.abs(B64).T)
     mid = (got + ora) / 2
     assert np.all(np.abs(exact[diff] - mid[diff]) <= err_bound[diff] + 1e-30)
     return int(diff.sum())
@@ -59,8 +59,8 @@ def test_local_select(L, small, M, T, k):
     case["h"] = small["h"][:M]
     W, A, B, h, tok = _dev(case)
     ids, sc = L.lowrank_score_topk(L.LOCAL, A, B, h, tok, T, k, with_scores=True)
-    _, S, _ = oracle_scores(case)
-    P.check_ids("local", host(ids), S, case["tok"], T, k)
+    _, S, _, SL = oracle_scores(case, with_slack=True)
+    P.check_ids("local", host(ids), S, case["tok"], T, k, slack_pos=SL)
     P.check_order("local", host(ids), host(sc), T, k, case["n"])
     assert ids.shape[1] == O.local_candidate_count(case["n"], T, k)
 
@@ -72,8 +72,8 @@ def test_global_select(L, small, M, C):
     case["h"] = small["h"][:M]
     W, A, B, h, tok = _dev(case)
     ids, sc = L.lowrank_score_topk(L.GLOBAL, A, B, h, tok, C, with_scores=True)
-    _, S, _ = oracle_scores(case)
-    P.check_ids("global", host(ids), S, case["tok"], C)
+    _, S, _, SL = oracle_scores(case, with_slack=True)
+    P.check_ids("global", host(ids), S, case["tok"], C, slack_pos=SL)
     P.check_order("global", host(ids), host(sc), C, 0, case["n"])
 
 
@@ -81,10 +81,10 @@ def test_global_select_long_rows(L):
     # rows long enough for the multi-pass radix path (> 8192 keys)
     case = make_case(20000, 64, 16, 3, seed=12)
     W, A, B, h, tok = _dev(case)
-    _, S, _ = oracle_scores(case)
+    _, S, _, SL = oracle_scores(case, with_slack=True)
     for C in (1, 100, 1024, 4096):
         ids = L.lowrank_score_topk(L.GLOBAL, A, B, h, tok, C)
-        P.check_ids("global", host(ids), S, case["tok"], C)
+        P.check_ids("global", host(ids), S, case["tok"], C, slack_pos=SL)
 
 
 def test_scores_match_oracle(L, small):
@@ -109,9 +109,9 @@ def test_two_stage(L, mode, C, k, temp):
     W, A, B, h, tok = _dev(case)
     md = L.LOCAL if mode == "local" else L.GLOBAL
     ids, lg, q = L.two_stage(md, W, A, B, h, tok, C, k, temperature=temp)
-    _, S, h64 = oracle_scores(case)
+    _, S, h64, SL = oracle_scores(case, with_slack=True)
     ids = host(ids)
-    P.check_ids(mode, ids, S, case["tok"], C, k)
+    P.check_ids(mode, ids, S, case["tok"], C, k, slack_pos=SL)
     ex = P.exact_logits(case["W"], h64, ids)
     P.check_logits(host(lg), ex)
     P.check_q(host(q), ex, temp)
@@ -121,8 +121,8 @@ def test_two_stage_identity_token_ids(L):
     case = make_case(1024, 64, 16, 2, seed=14, shuffle=False)
     W, A, B, h, _ = _dev(case)
     ids, lg, q = L.two_stage(L.LOCAL, W, A, B, h, None, 128, 4)
-    _, S, h64 = oracle_scores(case)
-    P.check_ids("local", host(ids), S, np.arange(1024), 128, 4)
+    _, S, h64, SL = oracle_scores(case, with_slack=True)
+    P.check_ids("local", host(ids), S, np.arange(1024), 128, 4, slack_pos=SL)
     ex = P.exact_logits(case["W"], h64, host(ids))
     P.check_logits(host(lg), ex)
     P.check_q(host(q), ex)

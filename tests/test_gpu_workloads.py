@@ -46,8 +46,8 @@ def _check(case, mode, C, k, ids, lg, q, rows=None):
     rows = np.arange(case["M"]) if rows is None else np.asarray(rows)
     sub = dict(case)
     sub["h"] = case["h"][rows]
-    _, S, h64 = oracle_scores(sub)
-    excused = P.check_ids(mode, ids[rows], S, case["tok"], C, k)
+    _, S, h64, SL = oracle_scores(sub, with_slack=True)
+    excused = P.check_ids(mode, ids[rows], S, case["tok"], C, k, slack_pos=SL)
     ex = P.exact_logits(case["W"], h64, ids[rows])
     floor = P.check_logits(lg[rows], ex)
     P.check_q(q[rows], ex)
