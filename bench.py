@@ -278,7 +278,7 @@ def run_ours(args):
             wsb.data_ptr(), wsb.numel(), handles, nl + 1,
             torch.cuda.current_stream().cuda_stream), "two_stage_profiled")
 
-    names = ["project_u", "score_local_topk", "gather_logits_softmax"][:nl]
+    names = ["project_u", "score_local_topk", "gather_logits", "candidate_softmax"][:nl]
     samples = {k: [] for k in names}
     prof_mode = "stream, events between the launches of one call"
     for i in range(args.steps):
@@ -294,7 +294,8 @@ def run_ours(args):
     bytes_kernel = {
         "project_u": 2 * r * d + 2 * M * d + 2 * M * r,
         "score_local_topk": 2 * n * r + 2 * M * r + 4 * M * K,
-        "gather_logits_softmax": 2 * d * U + 2 * M * d + 4 * M * K + 8 * M * K,
+        "gather_logits": 2 * d * U + 2 * M * d + 4 * M * K + 4 * M * K,
+        "candidate_softmax": 4 * M * K + 4 * M * K,
     }
     step_bytes = 2 * n * r + 2 * r * d + 2 * M * d + 2 * d * U + 12 * M * K
     hbm, peak_kind = peaks()

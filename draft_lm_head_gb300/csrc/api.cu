@@ -153,7 +153,7 @@ int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
   return LMHEAD_OK;
 }
 
-int launches_for(int mode, int k_tile) { return needs_score_buffer(mode, k_tile) ? 4 : 3; }
+int launches_for(int mode, int k_tile) { return needs_score_buffer(mode, k_tile) ? 5 : 4; }
 
 bool valid_temperature(float t) { return t > 0.f && isfinite(t); }
 
@@ -264,9 +264,11 @@ static int two_stage_impl(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
                   L, true, mk, s);
   if (st != LMHEAD_OK) return st;
   const int K = (int)candidate_count(mode, n, C_or_tile, k_tile);
-  cudaError_t e = launch_gather_logits(W, h, out_ids, n, d, M, K, out_logits, out_q,
-                                       1.f / temperature, reinterpret_cast<int*>(ws + L.tickets),
-                                       device_error_word(), s);
+  // stage 2: exact logits of the candidates, then their softmax (one CTA per row)
+  cudaError_t e = launch_gather_logits(W, h, out_ids, n, d, M, K, out_logits, nullptr, 1.f,
+                                       nullptr, device_error_word(), s);
+  if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
+  e = launch_row_softmax(out_logits, M, K, 1.f / temperature, out_q, s);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   return LMHEAD_OK;
 }

@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(256) project_u_kernel(const bf16_t* __restrict
                                                         int M, bf16_t* __restrict__ u,
                                                         int* zero_ptr, int zero_ints) {
   __shared__ uint4 hs[kMB * kDChunk / 8];
+  pdl_trigger();
   if (zero_ptr) {
     const int nb = gridDim.x * gridDim.y, bid = blockIdx.y * gridDim.x + blockIdx.x;
     for (int i = bid * blockDim.x + threadIdx.x; i < zero_ints; i += nb * blockDim.x) zero_ptr[i] = 0;
@@ -102,6 +103,7 @@ project_u_tc_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_const
   const int KS = gridDim.x;
   const int ks = blockIdx.x, rs = blockIdx.y, hc = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();  // the scoring kernel may start streaming A now
 
   if (zero_ptr) {
     const int nb = gridDim.x * gridDim.y * gridDim.z;
@@ -175,8 +177,13 @@ project_u_tc_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_const
     const int m = hc * kTcHid + rr, col = rs * kTcN + c;
     if (m >= M || col >= r) continue;
     const uint32_t off = red_addr + (uint32_t)(rr * kRedPitch + c) * 4u;
+    float part[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)  // all remote loads in flight, summed in rank order
+      part[q] = q < KS ? tc::ld_cluster_f32(tc::map_to_rank(off, (uint32_t)q)) : 0.f;
     float acc = 0.f;
-    for (int q = 0; q < KS; ++q) acc += tc::ld_cluster_f32(tc::map_to_rank(off, (uint32_t)q));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc += part[q];
     const __nv_bfloat16 b = __float2bfloat16_rn(acc);
     u[(size_t)m * r + col] = *reinterpret_cast<const bf16_t*>(&b);
   }

@@ -57,7 +57,9 @@ struct Params {
   int r, M, T, k_tile, K;
   int64_t n_chunks, tiles;
   int G, stages;
-  int lane_shift;  // 64 when M <= 64: hidden rows sit in TMEM lanes 64..127
+  int lane_shift;  // R == 1 and M <= 64: hidden rows sit in TMEM lanes 64..127
+  int R;           // copies of the hidden rows across the 128 TMEM lanes (1, 2, 4)
+  int rows_per_rep;  // 128 / R
   int32_t* out_ids;
   float* out_scores;
   float2* partials;   // [HC][G][2][kHid][KT]
@@ -167,6 +169,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
   const int kblocks = (p.r + kKBlock - 1) / kKBlock;
   uint8_t* u_s = dsmem;
   uint8_t* stage_s = dsmem + (size_t)kblocks * kStageBytes;
+  float2* xchg = reinterpret_cast<float2*>(stage_s + (size_t)p.stages * kStageBytes);  // [128][KT]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x, y = blockIdx.y;
@@ -203,15 +206,26 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
     if (lane == 0) {
       tc::prefetch_tmap(&amap);
       tc::prefetch_tmap(&umap);
-      asm volatile("griddepcontrol.wait;" ::: "memory");  // u comes from the previous kernel
-      tc::mbar_arrive_expect_tx(&ctl.ufull, (uint32_t)(kblocks * kStageBytes));
-      for (int kb = 0; kb < kblocks; ++kb)
-        tc::tma_load_2d(u_s + (size_t)kb * kStageBytes, &umap, &ctl.ufull, kb * kKBlock,
-                        y * kHid - p.lane_shift);  // rows before 0 are zero-filled
       uint32_t it = 0;
       bool ok = true;
-      for (int i = 0; i < nch && ok; ++i) {
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+      // A does not depend on the previous kernel: fill the ring first, then
+      // wait for u (written by the projection kernel) and load it
+      const uint32_t total_it = (uint32_t)nch * kblocks;
+      const uint32_t pre = total_it < (uint32_t)NS ? total_it : (uint32_t)NS;
+      for (; it < pre; ++it) {
+        const int s = (int)it;
+        tc::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
+        tc::tma_load_2d(stage_s + (size_t)s * kStageBytes, &amap, &ctl.full[s],
+                        (int)(it % kblocks) * kKBlock, (int)((c0 + it / kblocks) * kChunk));
+      }
+      pdl_wait();
+      tc::mbar_arrive_expect_tx(&ctl.ufull, (uint32_t)(kblocks * kStageBytes));
+      for (int kb = 0; kb < kblocks; ++kb)
+        for (int rep = 0; rep < p.R; ++rep)  // R copies; rows before 0 / past M are zero
+          tc::tma_load_2d(u_s + (size_t)kb * kStageBytes + (size_t)rep * p.rows_per_rep * 128, &umap,
+                          &ctl.ufull, kb * kKBlock, y * p.rows_per_rep - p.lane_shift);
+      for (int i = (int)(it / kblocks); i < nch && ok; ++i) {
+        for (int kb = (i == (int)(it / kblocks)) ? (int)(it % kblocks) : 0; kb < kblocks; ++kb, ++it) {
           const int s = (int)(it % NS);
           if (!tc::mbar_wait(&ctl.empty[s], ((it / NS) & 1) ^ 1, abort_flag)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
@@ -268,11 +282,13 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();  // tile tickets are zeroed by the projection kernel
     const int q = warp & 3;  // TMEM lane quadrant this warp may read
     const int ml = q * 32 + lane;
-    const int m = y * kHid + ml - p.lane_shift;
+    const int rep = (q * 32) / p.rows_per_rep;  // which copy of the hidden rows
+    const int m = y * p.rows_per_rep + ml % p.rows_per_rep - p.lane_shift;
     const bool valid = m >= 0 && m < p.M;
+    const bool valid_out = valid && rep == 0;  // copy 0 publishes the results
     const int64_t n = p.n, T = p.T;
     const int64_t P0 = c0 * kChunk;
     const int64_t P1 = min(n, c1 * kChunk);
@@ -296,8 +312,85 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
     };
     bool ok = true;
     // warps whose 32 hidden rows all lie outside [0, M) only pace the ring
-    const int m_lo = y * kHid + q * 32 - p.lane_shift;
+    const int m_lo = y * p.rows_per_rep + (q * 32) % p.rows_per_rep - p.lane_shift;
     const bool warp_live = m_lo + 31 >= 0 && m_lo < p.M;
+    if (p.R > 1) {
+      // T % 128 == 0: tiles end on chunk edges. Copy `rep` of the rows scans
+      // columns [rep*cols, (rep+1)*cols) of every chunk; at a tile end the
+      // copies' lists meet in shared memory and copy 0 combines them.
+      const int cols = kChunk / p.R;
+      const int jb = rep * cols;
+      const int qstep = p.rows_per_rep / 32;
+      for (int i = 0; i < nch; ++i) {
+        const int a = i & 1;
+        int okw = 1;
+        if (lane == 0) {
+          okw = ok && tc::mbar_wait(&ctl.acc_full[a], (i >> 1) & 1, abort_flag) ? 1 : 0;
+          if (!okw) *abort_flag = 1;
+        }
+        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+        ok = ok && okw;  // keep iterating on failure: the barriers below need every warp
+        tc::fence_after_sync();
+        const int64_t cbase = (c0 + i) * kChunk;
+        for (int j0 = jb; j0 < jb + cols && warp_live && ok; j0 += 32) {
+          const int64_t base = cbase + j0;
+          if (base >= P1) break;
+          uint32_t v[32];
+          tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kChunk + j0), v);
+          tc::tmem_ld_wait();
+          const int lim = (int)min((int64_t)32, P1 - base);
+          uint32_t ties = 0;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const bool t = sub[jj % kSub].push_fast(
+                jj < lim && valid ? __uint_as_float(v[jj]) : kNaN, (int32_t)(base + jj));
+            ties |= (t ? 1u : 0u) << jj;
+          }
+          if (ties != 0) {
+            float rest[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) rest[jj] = __uint_as_float(v[jj]);
+            for (uint32_t t = ties; t; t &= t - 1) {
+              const int jj = __ffs(t) - 1;
+              sub[0].push_exact(rest[jj], (int32_t)(base + jj), p.token_ids, n);
+            }
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&ctl.acc_empty[a]);
+        const int64_t cend = min(P1, cbase + kChunk);
+        const int64_t ctile = cbase / T;
+        if (cend == min(n, ctile * T + T) || cend == P1) {  // this chunk ends a tile
+          RegList<KT, true> Lst = merged();
+#pragma unroll
+          for (int j = 0; j < KT; ++j)
+            xchg[ml * KT + j] = make_float2(Lst.s[j], __int_as_float(Lst.k[j]));
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (rep == 0) {
+            for (int r2 = 1; r2 < p.R; ++r2) {
+              const int ol = (q + r2 * qstep) * 32 + lane;
+#pragma unroll
+              for (int j = 0; j < KT; ++j) {
+                const float2 e = xchg[ol * KT + j];
+                Lst.push_exact(e.x == -INFINITY ? kNaN : e.x, __float_as_int(e.y), p.token_ids, n);
+              }
+            }
+            if (cend == P1) {
+              cur = Lst;  // the range's last tile: the code below decides
+            } else if (ctile == first_tile && first_partial) {
+              first = Lst;  // part of a tile cut by this CTA's start
+            } else if (valid_out && ok) {
+              write_tile<KT>(p, m, ctile, (int)min((int64_t)KT, min(n, ctile * T + T) - ctile * T),
+                             Lst, true);
+            }
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll
+          for (int j = 0; j < kSub; ++j) sub[j].reset();
+        }
+      }
+    } else {
     for (int i = 0; i < nch; ++i) {
       const int a = i & 1;
       int okw = 1;
@@ -352,6 +445,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       if (lane == 0) tc::mbar_arrive(&ctl.acc_empty[a]);
     }
     cur = merged();
+    }
 
     // ---- tiles cut by CTA boundaries: publish parts, last part merges.
     // Which tiles are cut depends only on this CTA's range [P0, P1).
@@ -362,9 +456,9 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
     int64_t part_tile[2] = {first_cut ? first_tile : -1, last_cut ? last_tile : -1};
     // the running list now holds the last tile; complete unless cut
     const bool last_is_cut = (last_tile == first_tile) ? first_cut : last_cut;
-    if (ok && valid && !last_is_cut)
+    if (ok && valid_out && !last_is_cut)
       write_tile<KT>(p, m, last_tile, (int)min((int64_t)KT, last_end - last_tile * T), cur, true);
-    if (ok && valid) {
+    if (ok && valid_out) {
       for (int side = 0; side < 2; ++side) {
         if (part_tile[side] < 0) continue;
         const RegList<KT, true>& src = (side == 0 && last_tile != first_tile) ? first : cur;
@@ -395,7 +489,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       if (!ctl.decision[side]) continue;
       const int64_t t = part_tile[side];
       __threadfence();
-      if (valid) {
+      if (valid_out) {
         const int64_t fc = t * T / kChunk;
         const int64_t lc = (min(n, t * T + T) - 1) / kChunk;
         const int64_t b0 = cta_of_chunk(fc, p.n_chunks, p.G), b1 = cta_of_chunk(lc, p.n_chunks, p.G);
@@ -436,8 +530,8 @@ cudaError_t launch_kt(const CUtensorMap& amap, const CUtensorMap& umap, const Pa
   static int smem_set[64] = {0};
   cudaError_t e = ensure_dynamic_smem(local_topk_tc_kernel<KT>, smem, smem_set);
   if (e != cudaSuccess) return e;
-  local_topk_tc_kernel<KT><<<dim3(p.G, HC), kThreads, smem, s>>>(amap, umap, p);
-  return cudaGetLastError();
+  return launch_kernel(true, local_topk_tc_kernel<KT>, dim3(p.G, HC), dim3(kThreads), smem, s, amap,
+                       umap, p);
 }
 
 }  // namespace
@@ -480,11 +574,14 @@ cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t
   const int kblocks = (r + kKBlock - 1) / kKBlock;
   const size_t u_bytes = (size_t)kblocks * kStageBytes;
   const size_t budget = 232448 - 2048;  // opt-in shared memory minus static + alignment slack
-  int stages = (int)((budget - 1024 - u_bytes) / kStageBytes);
+  const size_t xchg_bytes = (size_t)kHid * 8 * sizeof(float2);
+  int stages = (int)((budget - 1024 - u_bytes - xchg_bytes) / kStageBytes);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return cudaErrorInvalidValue;
   p.stages = stages;
-  p.lane_shift = M <= 64 ? 64 : 0;
+  p.R = (T % kChunk == 0) ? (M <= 32 ? 4 : (M <= 64 ? 2 : 1)) : 1;
+  p.rows_per_rep = kHid / p.R;
+  p.lane_shift = (p.R == 1 && M <= 64) ? 64 : 0;
   p.out_ids = out_ids;
   p.out_scores = out_scores;
   p.partials = static_cast<float2*>(partials);
@@ -492,10 +589,10 @@ cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t
   p.err = err;
   CUtensorMap amap, umap;
   if (!make_bf16_map(&amap, A, (uint64_t)n, (uint64_t)r, kChunk, kKBlock) ||
-      !make_bf16_map(&umap, u, (uint64_t)M, (uint64_t)r, kHid, kKBlock))
+      !make_bf16_map(&umap, u, (uint64_t)M, (uint64_t)r, p.rows_per_rep, kKBlock))
     return cudaErrorInvalidValue;
-  const int HC = (M + kHid - 1) / kHid;
-  const size_t smem = 1024 + u_bytes + (size_t)stages * kStageBytes;
+  const int HC = (M + p.rows_per_rep - 1) / p.rows_per_rep;
+  const size_t smem = 1024 + u_bytes + (size_t)stages * kStageBytes + xchg_bytes;
   switch (k_tile) {
     case 1: return launch_kt<1>(amap, umap, p, HC, smem, s);
     case 2: return launch_kt<2>(amap, umap, p, HC, smem, s);
