@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--rotations", type=int, default=NROT,
+                   help="input copies cycled through (>= 4 keeps every read cold in L2)")
     return p.parse_args()
 
 
@@ -72,6 +74,26 @@ def head_inputs(wl=WORKLOAD):
 def hidden(W, M, rank):
     h, _ = synth.make_hidden(W, M, WORKLOAD.index, stream_offset=rank)
     return h
+
+
+def ncu_traffic(kernel, M):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture, or None
+    when the capture was taken at another M or the kernel's source changed."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh).get(kernel)
+    if not rec or rec.get("M") != M:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as fh:
+        if hashlib.sha1(fh.read()).hexdigest() != rec["source_sha1"]:
+            return None
+    return int(rec["dram_bytes"])
 
 
 def peaks():
@@ -180,6 +202,8 @@ def make_graph(torch, fn):
 
 def run_ours(args):
     import ctypes
+    global NROT
+    NROT = max(1, args.rotations)
 
     import torch
     import torch.distributed as dist
@@ -303,7 +327,8 @@ def run_ours(args):
     achieved = bytes_kernel[dom] / (kern_us[dom] * 1e-6) / 1e9
     roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
             "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
-            "bytes_per_launch": bytes_kernel[dom], "traffic": None, "timing": prof_mode}
+            "bytes_per_launch": bytes_kernel[dom], "traffic": ncu_traffic(dom, M),
+            "timing": prof_mode}
 
     # end to end through the public API: host buffers, copies inside the timed region
     h_host = [torch.from_numpy(np.ascontiguousarray(hb).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -390,7 +415,7 @@ def run_ours(args):
                                    "fused local top-k tile=256 k_tile=2",
                        "n": n, "d": d, "r": r, "M": M, "mode": "local", "tile": wl.T,
                        "k_tile": wl.k_tile, "candidates": K,
-                       "l2": f"{NROT} rotating copies of every input (> 2x L2)",
+                       "l2": f"{NROT} rotating copies of every input" + (" (> 2x L2)" if NROT >= 4 else ""),
                        "launch": "CUDA graph replay of library calls",
                        "parallelism": f"replicas x{world} (independent hidden vectors)"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
