@@ -280,6 +280,51 @@ row_softmax_kernel(const float* __restrict__ L, int64_t K, float inv_temp, float
   for (int64_t j = tid; j < K; j += blockDim.x) qrow[j] = __expf(row[j] * inv_temp - gm) * inv;
 }
 
+// Rows of up to 256 * EPT logits: every element is read once into registers,
+// the row max and sum are block reductions, and q is written from registers.
+template <int EPT>
+__global__ void __launch_bounds__(256)
+row_softmax_reg_kernel(const float* __restrict__ L, int K, float inv_temp, float* __restrict__ q) {
+  __shared__ float red[8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();  // the logits come from the previous kernel
+  const float* row = L + (size_t)blockIdx.x * K;
+  float* qrow = q + (size_t)blockIdx.x * K;
+  float z[EPT];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int j = tid + 256 * e;
+    z[e] = j < K ? row[j] * inv_temp : -INFINITY;
+    mx = fmaxf(mx, z[e]);
+  }
+  mx = warp_max(mx);
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  float gm = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) gm = fmaxf(gm, red[w]);
+  __syncthreads();  // red is reused below
+  float sum = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    z[e] = __expf(z[e] - gm);  // exp(-inf) = 0 for padding
+    sum += z[e];
+  }
+  sum = warp_sum(sum);
+  if (lane == 0) red[warp] = sum;
+  __syncthreads();
+  float gs = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) gs += red[w];
+  const float inv = 1.f / gs;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int j = tid + 256 * e;
+    if (j < K) qrow[j] = z[e] * inv;
+  }
+}
+
 }  // namespace
 
 template <int VPL>
@@ -321,6 +366,12 @@ cudaError_t launch_gather_logits(const bf16_t* W, const bf16_t* h, const int32_t
 
 cudaError_t launch_row_softmax(const float* L, int M, int64_t K, float inv_temp, float* q,
                                cudaStream_t s) {
+  if (K <= 256 * 4)
+    return launch_kernel(true, row_softmax_reg_kernel<4>, dim3(M), dim3(256), 0, s, L, (int)K,
+                         inv_temp, q);
+  if (K <= 256 * 16)
+    return launch_kernel(true, row_softmax_reg_kernel<16>, dim3(M), dim3(256), 0, s, L, (int)K,
+                         inv_temp, q);
   return launch_kernel(true, row_softmax_kernel, dim3(M), dim3(256), 0, s, L, K, inv_temp, q);
 }
 

@@ -194,10 +194,80 @@ project_u_tc_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_const
   }
 }
 
+// ---------------------------------------------------------------- small M
+// GEMV form for a few hidden vectors: one CTA per row k of B; each thread
+// loads its slice of B[k] and of every h[m] at once (everything in flight
+// together), then one block reduction per hidden vector. Latency-bound by
+// design: a single round trip to memory.
+constexpr int kGemvThreads = 128;
+constexpr int kGemvMaxM = 8;
+
+// VPT 16-byte vectors per thread cover d <= VPT * 1024; up to MM hidden vectors.
+template <int VPT, int MM>
+__global__ void __launch_bounds__(kGemvThreads)
+project_u_gemv_kernel(const bf16_t* __restrict__ B, const bf16_t* __restrict__ h, int d, int r,
+                      int M, bf16_t* __restrict__ u, int* zero_ptr, int zero_ints) {
+  constexpr int kGemvMaxVpt = VPT;
+  __shared__ float red[kGemvMaxM][kGemvThreads / 32];
+  pdl_trigger();  // the scoring kernel may start streaming A now
+  if (zero_ptr) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < zero_ints; i += gridDim.x * blockDim.x)
+      zero_ptr[i] = 0;
+  }
+  const int k = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nvec = d >> 3;
+  const uint4* brow = reinterpret_cast<const uint4*>(B + (size_t)k * d);
+  uint4 bv[kGemvMaxVpt];
+  uint4 hv[MM][kGemvMaxVpt];
+#pragma unroll
+  for (int i = 0; i < kGemvMaxVpt; ++i) {
+    const int v = tid + kGemvThreads * i;
+    bv[i] = v < nvec ? ldg_nc_v4(brow + v) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int mm = 0; mm < MM; ++mm) {
+    const uint4* hrow = reinterpret_cast<const uint4*>(h + (size_t)mm * d);
+#pragma unroll
+    for (int i = 0; i < kGemvMaxVpt; ++i) {
+      const int v = tid + kGemvThreads * i;
+      hv[mm][i] = (mm < M && v < nvec) ? __ldg(hrow + v) : make_uint4(0, 0, 0, 0);
+    }
+  }
+#pragma unroll
+  for (int mm = 0; mm < MM; ++mm) {
+    if (mm < M) {
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < kGemvMaxVpt; ++i) acc += dot8(bv[i], hv[mm][i]);
+      acc = warp_sum(acc);
+      if (lane == 0) red[mm][warp] = acc;
+    }
+  }
+  __syncthreads();
+  if (tid < M) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kGemvThreads / 32; ++w) s += red[tid][w];
+    const __nv_bfloat16 b = __float2bfloat16_rn(s);
+    u[(size_t)tid * r + k] = *reinterpret_cast<const bf16_t*>(&b);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int M, bf16_t* u,
                              int* zero_ptr, int zero_ints, cudaStream_t s) {
+  if (M <= kGemvMaxM && d <= 8192) {
+    const int vpt = (d + 1023) / 1024;
+    if (vpt <= 1) project_u_gemv_kernel<1, 8><<<r, kGemvThreads, 0, s>>>(B, h, d, r, M, u, zero_ptr, zero_ints);
+    else if (vpt <= 2) project_u_gemv_kernel<2, 8><<<r, kGemvThreads, 0, s>>>(B, h, d, r, M, u, zero_ptr, zero_ints);
+    else if (vpt <= 4) project_u_gemv_kernel<4, 8><<<r, kGemvThreads, 0, s>>>(B, h, d, r, M, u, zero_ptr, zero_ints);
+    else if (M <= 4) project_u_gemv_kernel<8, 4><<<r, kGemvThreads, 0, s>>>(B, h, d, r, M, u, zero_ptr, zero_ints);
+    else goto tensor_cores;
+    return cudaGetLastError();
+  }
+tensor_cores:
   if (d <= kProjTcMaxD) {
     // d split over a cluster of KS <= 8 CTAs, slices of a multiple of 64 columns
     const int KS = min(8, (d + 511) / 512);

@@ -11,14 +11,17 @@
 //  - u (128 hidden vectors x r, zero-filled past M) is loaded once by TMA and
 //    is the MMA's A operand; the chunk is the B operand (N = 128). One
 //    elected thread issues tcgen05.mma (M=128, N=128, K=16, fp32 in TMEM)
-//    into two TMEM accumulators, so the epilogue of chunk i overlaps the
-//    MMAs of chunk i+1.
+//    into four TMEM accumulators, so the MMAs run up to four chunks ahead of
+//    the epilogue.
 //  - Epilogue: 4 warps; thread t owns TMEM lane t = one hidden vector and
 //    reads its 128 scores with tcgen05.ld, keeping a sorted top-k_tile list
 //    of (score, position) in registers. A tile boundary flushes the list:
 //    ids are written through token_ids (ties: smaller vocabulary id).
-//  - A tile cut by a CTA boundary leaves partial lists in the workspace; the
-//    last CTA to finish a part (atomic ticket, no waiting) merges them.
+//  - Tiles of a multiple of 128 rows (the usual case) are scheduled
+//    dynamically, whole tiles per CTA (local_topk_tc_dyn_kernel). Otherwise
+//    CTAs take balanced contiguous chunk ranges; a tile cut by a CTA boundary
+//    leaves partial lists in the workspace and the last CTA to finish a part
+//    (atomic ticket, no waiting) merges them.
 //  - Every mbarrier wait is bounded; on timeout the CTA raises an abort flag,
 //    records LMHEAD_ERR_TIMEOUT in the device error word, drains its own TMA
 //    copies, frees TMEM and exits.
@@ -37,15 +40,16 @@ constexpr int kKBlock = 64;                 // bf16 per 128-byte swizzled row
 constexpr int kStageBytes = kChunk * 128;   // one 128-row x 64-element box
 constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kMaxStages = 12;
-constexpr int kTmemCols = 256;              // two 128-column fp32 accumulators
+constexpr int kAcc = 4;                     // TMEM accumulators (the MMA runs ahead)
+constexpr int kTmemCols = kAcc * 128;       // 128 fp32 columns each
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kHid, kChunk);
 
 struct SharedCtl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t ufull;
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+  uint64_t acc_full[kAcc];
+  uint64_t acc_empty[kAcc];
   uint32_t tmem_base;
   int abort;
   int decision[2];
@@ -185,7 +189,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       tc::mbar_init(&ctl.empty[s], 1);
     }
     tc::mbar_init(&ctl.ufull, 1);
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kAcc; ++a) {
       tc::mbar_init(&ctl.acc_full[a], 1);
       tc::mbar_init(&ctl.acc_empty[a], 4);
     }
@@ -257,8 +261,8 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       bool ok = tc::mbar_wait(&ctl.ufull, 0, abort_flag);
       uint32_t it = 0;
       for (int i = 0; i < nch && ok; ++i) {
-        const int a = i & 1;
-        if (!tc::mbar_wait(&ctl.acc_empty[a], ((i >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        const int a = i % kAcc;
+        if (!tc::mbar_wait(&ctl.acc_empty[a], ((i / kAcc) & 1) ^ 1, abort_flag)) { ok = false; break; }
         tc::fence_after_sync();
         const uint32_t d = tmem + a * kChunk;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
@@ -322,10 +326,10 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       const int jb = rep * cols;
       const int qstep = p.rows_per_rep / 32;
       for (int i = 0; i < nch; ++i) {
-        const int a = i & 1;
+        const int a = i % kAcc;
         int okw = 1;
         if (lane == 0) {
-          okw = ok && tc::mbar_wait(&ctl.acc_full[a], (i >> 1) & 1, abort_flag) ? 1 : 0;
+          okw = ok && tc::mbar_wait(&ctl.acc_full[a], (i / kAcc) & 1, abort_flag) ? 1 : 0;
           if (!okw) *abort_flag = 1;
         }
         okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
@@ -392,9 +396,9 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       }
     } else {
     for (int i = 0; i < nch; ++i) {
-      const int a = i & 1;
+      const int a = i % kAcc;
       int okw = 1;
-      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (i >> 1) & 1, abort_flag) ? 1 : 0;
+      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (i / kAcc) & 1, abort_flag) ? 1 : 0;
       okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
       if (!okw) { ok = false; break; }
       tc::fence_after_sync();
@@ -523,10 +527,306 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
   }
 }
 
+// ---------------------------------------------------------------- dynamic tiles
+// Variant for tiles of a multiple of 128 rows: whole tiles are the unit of
+// work. CTA b first takes tile b (so it can stream A before the projection
+// kernel finishes), then claims tiles G, G+1, ... from a counter in the
+// workspace (zeroed by the projection kernel), so SMs that get their data
+// faster take more tiles. Chunk descriptors reach the MMA and epilogue
+// warps through a shared ring; no tile is ever split between CTAs.
+constexpr int kDescRing = 32;  // > stages + accumulators: the producer is never a ring ahead
+
+// All 128 epilogue threads agree: true only if every one passes true.
+__device__ __forceinline__ bool epilogue_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+template <int KT>
+__global__ void __launch_bounds__(kThreads, 1)
+local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
+                         const __grid_constant__ CUtensorMap umap, const Params p) {
+  extern __shared__ uint8_t dsmem_raw[];
+  __shared__ SharedCtl ctl;
+  __shared__ int desc_tile[kDescRing], desc_chunk[kDescRing];
+  uint8_t* dsmem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int kblocks = (p.r + kKBlock - 1) / kKBlock;
+  uint8_t* u_s = dsmem;
+  uint8_t* stage_s = dsmem + (size_t)kblocks * kStageBytes;
+  float2* xchg = reinterpret_cast<float2*>(stage_s + (size_t)p.stages * kStageBytes);  // [128][KT]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int y = blockIdx.y;
+  const int NS = p.stages;
+  const int64_t n = p.n, T = p.T;
+  const int cpt = (int)(T / kChunk);  // chunks per tile
+  int* counter = p.tile_tickets + y;
+  volatile int* abort_flag = &ctl.abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      tc::mbar_init(&ctl.full[s], 1);
+      tc::mbar_init(&ctl.empty[s], 1);
+    }
+    tc::mbar_init(&ctl.ufull, 1);
+    for (int a = 0; a < kAcc; ++a) {
+      tc::mbar_init(&ctl.acc_full[a], 1);
+      tc::mbar_init(&ctl.acc_empty[a], 4);
+    }
+    ctl.abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&ctl.tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&amap);
+      tc::prefetch_tmap(&umap);
+      uint32_t it = 0;  // stage sequence
+      int c = 0;        // chunk sequence
+      bool ok = true, u_loaded = false;
+      int64_t tile = blockIdx.x < p.tiles ? (int64_t)blockIdx.x : -1;
+      int64_t next = -1;
+      while (ok) {
+        if (tile >= 0 && u_loaded && next < 0) {
+          // claim the tile after this one early; its value is needed later
+          next = (int64_t)p.G + atomicAdd(counter, 1);
+        }
+        const int slot = c % kDescRing;
+        if (tile < 0 || tile >= p.tiles) {  // no more work: an end marker through the ring
+          const int s = (int)(it % NS);
+          if (it >= (uint32_t)NS && !tc::mbar_wait(&ctl.empty[s], ((it / NS) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          desc_tile[slot] = -1;
+          tc::mbar_arrive(&ctl.full[s]);
+          ++it;
+          break;
+        }
+        for (int j = 0; j < cpt && ok; ++j) {
+          const int64_t gc = tile * cpt + j;  // global chunk
+          if (gc * kChunk >= n) break;
+          const bool last = j == cpt - 1 || (gc + 1) * kChunk >= n;
+          desc_tile[c % kDescRing] = (int)tile;
+          desc_chunk[c % kDescRing] = j | (last ? (int)0x80000000 : 0);
+          for (int kb = 0; kb < kblocks; ++kb, ++it) {
+            const int s = (int)(it % NS);
+            if (it >= (uint32_t)NS && !tc::mbar_wait(&ctl.empty[s], ((it / NS) & 1) ^ 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
+            tc::tma_load_2d(stage_s + (size_t)s * kStageBytes, &amap, &ctl.full[s], kb * kKBlock,
+                            (int)(gc * kChunk));
+            if (!u_loaded && (it + 1 >= (uint32_t)NS || (j == cpt - 1 && kb == kblocks - 1))) {
+              // ring filled (or first tile issued): now wait for u, written by the previous kernel
+              pdl_wait();
+              tc::mbar_arrive_expect_tx(&ctl.ufull, (uint32_t)(kblocks * kStageBytes));
+              for (int ub = 0; ub < kblocks; ++ub)
+                for (int rep = 0; rep < p.R; ++rep)
+                  tc::tma_load_2d(u_s + (size_t)ub * kStageBytes + (size_t)rep * p.rows_per_rep * 128,
+                                  &umap, &ctl.ufull, ub * kKBlock, y * p.rows_per_rep - p.lane_shift);
+              u_loaded = true;
+            }
+          }
+          ++c;
+        }
+        if (!u_loaded) {  // no tile at all for this CTA
+          pdl_wait();
+          tc::mbar_arrive_expect_tx(&ctl.ufull, (uint32_t)(kblocks * kStageBytes));
+          for (int ub = 0; ub < kblocks; ++ub)
+            for (int rep = 0; rep < p.R; ++rep)
+              tc::tma_load_2d(u_s + (size_t)ub * kStageBytes + (size_t)rep * p.rows_per_rep * 128,
+                              &umap, &ctl.ufull, ub * kKBlock, y * p.rows_per_rep - p.lane_shift);
+          u_loaded = true;
+        }
+        if (tile >= 0 && next < 0) next = (int64_t)p.G + atomicAdd(counter, 1);
+        tile = next;
+        next = -1;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, kDevErrTimeout);
+      }
+      pdl_trigger();
+      if (*abort_flag) {
+        const uint32_t first = it > (uint32_t)NS ? it - NS : 0;
+        for (uint32_t jq = first; jq < it; ++jq) {
+          const long long t0 = clock64();
+          while (!tc::mbar_try_wait(&ctl.full[jq % NS], (jq / NS) & 1) &&
+                 clock64() - t0 < tc::kWaitCycles) {
+          }
+        }
+        const long long t0 = clock64();
+        while (u_loaded && !tc::mbar_try_wait(&ctl.ufull, 0) && clock64() - t0 < tc::kWaitCycles) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = tc::mbar_wait(&ctl.ufull, 0, abort_flag);
+      uint32_t it = 0;
+      for (int c = 0; ok; ++c) {
+        const int a = c % kAcc;
+        int s = (int)(it % NS);
+        if (!tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag)) { ok = false; break; }
+        if (desc_tile[c % kDescRing] < 0) {  // end marker: pass it on to the epilogue
+          tc::mbar_arrive(&ctl.acc_full[a]);
+          break;
+        }
+        if (!tc::mbar_wait(&ctl.acc_empty[a], ((c / kAcc) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t d = tmem + a * kChunk;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          s = (int)(it % NS);
+          if (kb > 0 && !tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint64_t adesc = tc::sw128_kmajor_desc(tc::smem_addr(u_s + (size_t)kb * kStageBytes));
+          const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_addr(stage_s + (size_t)s * kStageBytes));
+          const int nk = min(4, (p.r - kb * kKBlock + 15) / 16);
+          for (int k = 0; k < nk; ++k)
+            tc::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, (kb | k) != 0);
+          tc::mma_commit(&ctl.empty[s]);
+        }
+        if (!ok) break;
+        tc::mma_commit(&ctl.acc_full[a]);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, kDevErrTimeout);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    pdl_wait();
+    const int q = warp & 3;
+    const int ml = q * 32 + lane;
+    const int rep = (q * 32) / p.rows_per_rep;
+    const int m = y * p.rows_per_rep + ml % p.rows_per_rep - p.lane_shift;
+    const bool valid = m >= 0 && m < p.M;
+    const bool valid_out = valid && rep == 0;
+    const int m_lo = y * p.rows_per_rep + (q * 32) % p.rows_per_rep - p.lane_shift;
+    const bool warp_live = m_lo + 31 >= 0 && m_lo < p.M;
+    const float kNaN = __int_as_float(0x7FC00000);
+    const int cols = kChunk / p.R;
+    const int jb = rep * cols;
+    const int qstep = p.rows_per_rep / 32;
+    constexpr int kSub = KT <= 4 ? 4 : 2;
+    RegList<KT, true> sub[kSub];
+#pragma unroll
+    for (int j = 0; j < kSub; ++j) sub[j].reset();
+    for (int c = 0;; ++c) {
+      const int a = c % kAcc;
+      int okw = 1;
+      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (c / kAcc) & 1, abort_flag) ? 1 : 0;
+      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+      if (!epilogue_all(okw != 0)) {  // uniform: every epilogue warp leaves together
+        if (lane == 0) { *abort_flag = 1; record_error(p.err, kDevErrTimeout); }
+        break;
+      }
+      tc::fence_after_sync();
+      const int tile = desc_tile[c % kDescRing];
+      if (tile < 0) break;  // end marker (same for every warp)
+      const int dc = desc_chunk[c % kDescRing];
+      const int j = dc & 0x7FFFFFFF;
+      const bool last = dc < 0;
+      const int64_t cbase = ((int64_t)tile * cpt + j) * kChunk;
+      const int64_t cend = min(n, cbase + kChunk);
+      for (int j0 = jb; j0 < jb + cols && warp_live; j0 += 32) {
+        const int64_t base = cbase + j0;
+        if (base >= cend) break;
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kChunk + j0), v);
+        tc::tmem_ld_wait();
+        const int lim = (int)min((int64_t)32, cend - base);
+        uint32_t ties = 0;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const bool t = sub[jj % kSub].push_fast(
+              jj < lim && valid ? __uint_as_float(v[jj]) : kNaN, (int32_t)(base + jj));
+          ties |= (t ? 1u : 0u) << jj;
+        }
+        if (ties != 0) {
+          float rest[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) rest[jj] = __uint_as_float(v[jj]);
+          for (uint32_t t = ties; t; t &= t - 1) {
+            const int jj = __ffs(t) - 1;
+            sub[0].push_exact(rest[jj], (int32_t)(base + jj), p.token_ids, n);
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&ctl.acc_empty[a]);
+      if (last) {  // the tile is complete: combine the copies' lists and write it
+        RegList<KT, true> Lst = sub[0];
+#pragma unroll
+        for (int jj = 1; jj < kSub; ++jj) Lst.absorb(sub[jj], p.token_ids, n);
+        if (p.R > 1) {
+#pragma unroll
+          for (int jj = 0; jj < KT; ++jj)
+            xchg[ml * KT + jj] = make_float2(Lst.s[jj], __int_as_float(Lst.k[jj]));
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (rep == 0) {
+            for (int r2 = 1; r2 < p.R; ++r2) {
+              const int ol = (q + r2 * qstep) * 32 + lane;
+#pragma unroll
+              for (int jj = 0; jj < KT; ++jj) {
+                const float2 e = xchg[ol * KT + jj];
+                Lst.push_exact(e.x == -INFINITY ? kNaN : e.x, __float_as_int(e.y), p.token_ids, n);
+              }
+            }
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+        }
+        if (valid_out)
+          write_tile<KT>(p, m, tile, (int)min((int64_t)KT, min(n, (int64_t)(tile + 1) * T) - (int64_t)tile * T),
+                         Lst, true);
+#pragma unroll
+        for (int jj = 0; jj < kSub; ++jj) sub[jj].reset();
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 template <int KT>
 cudaError_t launch_kt(const CUtensorMap& amap, const CUtensorMap& umap, const Params& p, int HC,
                       size_t smem, cudaStream_t s) {
+  if (p.T % kChunk == 0) {
+    static int smem_set_dyn[64] = {0};
+    cudaError_t e = ensure_dynamic_smem(local_topk_tc_dyn_kernel<KT>, smem, smem_set_dyn);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(true, local_topk_tc_dyn_kernel<KT>, dim3(p.G, HC), dim3(kThreads), smem, s,
+                         amap, umap, p);
+  }
   static int smem_set[64] = {0};
   cudaError_t e = ensure_dynamic_smem(local_topk_tc_kernel<KT>, smem, smem_set);
   if (e != cudaSuccess) return e;
@@ -550,6 +850,7 @@ size_t local_topk_tc_scratch_bytes(int64_t n, int M, int T) {
 
 int local_topk_tc_tickets(int64_t n, int M, int T) {
   const int64_t HC = (M + kHid - 1) / kHid;
+  if (T % kChunk == 0) return (int)HC;  // one tile counter per hidden-row chunk
   return (int)(HC * ((n + T - 1) / T));
 }
 
@@ -570,7 +871,7 @@ cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t
   p.tiles = (n + T - 1) / T;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  p.G = (int)min((int64_t)min(sms, kLocalTcMaxCtas), p.n_chunks);
+  p.G = (int)min((int64_t)min(sms, kLocalTcMaxCtas), T % kChunk == 0 ? p.tiles : p.n_chunks);
   const int kblocks = (r + kKBlock - 1) / kKBlock;
   const size_t u_bytes = (size_t)kblocks * kStageBytes;
   const size_t budget = 232448 - 2048;  // opt-in shared memory minus static + alignment slack
