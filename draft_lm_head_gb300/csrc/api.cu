@@ -3,6 +3,7 @@
 // allocates device memory or synchronises (except lmhead_last_device_error).
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "common.cuh"
@@ -47,7 +48,18 @@ bool needs_score_buffer(int mode, int k_tile) {
   return mode == LMHEAD_GLOBAL || k_tile > kFusedMaxKTile;
 }
 
-Layout layout_for(int mode, int64_t n, int r, int M, int C_or_tile, int k_tile) {
+// Columns per block of the warp gather's candidate order in local mode (a
+// block of tiles); LMHEAD_GATHER_SPAN overrides it (0 = row by row).
+int gather_span(int k_tile) {
+  static int v = -2;
+  if (v == -2) {
+    const char* e = getenv("LMHEAD_GATHER_SPAN");
+    v = e ? atoi(e) : -1;
+  }
+  return v >= 0 ? v : 16 * k_tile;
+}
+
+Layout layout_for(int mode, int64_t n, int d, int r, int M, int C_or_tile, int k_tile) {
   Layout L;
   size_t off = 0;
   L.u = off;
@@ -144,7 +156,7 @@ int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
     return LMHEAD_OK;
   }
   float* S = reinterpret_cast<float*>(ws + L.scores);
-  e = launch_score_all_fma(A, u, n, r, M, S, s);
+  e = launch_rows_dense_tc(A, n, r, u, M, S, n, device_error_word(), s);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   const int64_t seg = mode == LMHEAD_GLOBAL ? n : C_or_tile;
   const int k = mode == LMHEAD_GLOBAL ? C_or_tile : k_tile;
@@ -188,7 +200,7 @@ int64_t lmhead_candidate_count(int mode, int64_t n, int C_or_tile, int k_tile) {
 size_t lmhead_workspace_size(int mode, int64_t n, int d, int r, int M, int C_or_tile,
                              int k_tile) {
   if (check_select(mode, n, d, r, M, C_or_tile, k_tile) != LMHEAD_OK) return 0;
-  return layout_for(mode, n, r, M, C_or_tile, k_tile).total;
+  return layout_for(mode, n, d, r, M, C_or_tile, k_tile).total;
 }
 
 int lmhead_project_u(const lmhead_bf16* B, const lmhead_bf16* h, int d, int r, int M,
@@ -212,7 +224,7 @@ int lmhead_lowrank_score_topk(int mode, const lmhead_bf16* A, const lmhead_bf16*
   if (!aligned16(A) || !aligned16(B) || !aligned16(h) || (token_ids && !aligned16(token_ids)) ||
       !aligned16(out_ids) || (out_scores && !aligned16(out_scores)))
     return LMHEAD_ERR_ALIGN;
-  const Layout L = layout_for(mode, n, r, M, C_or_tile, k_tile);
+  const Layout L = layout_for(mode, n, d, r, M, C_or_tile, k_tile);
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return LMHEAD_ERR_WORKSPACE;
   Marks none;
@@ -255,7 +267,7 @@ static int two_stage_impl(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
   if (!aligned16(W) || !aligned16(A) || !aligned16(B) || !aligned16(h) ||
       (token_ids && !aligned16(token_ids)) || !aligned16(out_ids))
     return LMHEAD_ERR_ALIGN;
-  const Layout L = layout_for(mode, n, r, M, C_or_tile, k_tile);
+  const Layout L = layout_for(mode, n, d, r, M, C_or_tile, k_tile);
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return LMHEAD_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
@@ -266,7 +278,8 @@ static int two_stage_impl(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
   const int K = (int)candidate_count(mode, n, C_or_tile, k_tile);
   // stage 2: exact logits of the candidates, then their softmax (one CTA per row)
   cudaError_t e = launch_gather_logits(W, h, out_ids, n, d, M, K, out_logits, nullptr, 1.f,
-                                       nullptr, device_error_word(), s);
+                                       nullptr, device_error_word(), s,
+                                       mode == LMHEAD_LOCAL ? gather_span(k_tile) : 0);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   e = launch_row_softmax(out_logits, M, K, 1.f / temperature, out_q, s);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
@@ -311,7 +324,7 @@ int lmhead_dense_head(const lmhead_bf16* W, const lmhead_bf16* h, int64_t n, int
   if (out_q && !valid_temperature(temperature)) return LMHEAD_ERR_SHAPE;
   if (!aligned16(W) || !aligned16(h)) return LMHEAD_ERR_ALIGN;
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_dense_logits(W, h, n, d, M, out_logits, s);
+  cudaError_t e = launch_rows_dense_tc(W, n, d, h, M, out_logits, n, device_error_word(), s);
   if (e != cudaSuccess || !out_q) return cuda_status(e);
   return cuda_status(launch_row_softmax(out_logits, M, n, 1.f / temperature, out_q, s));
 }

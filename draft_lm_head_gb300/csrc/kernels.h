@@ -51,17 +51,23 @@ cudaError_t launch_segment_topk(const float* S, const int32_t* token_ids, int64_
 
 // K5 (+K6 fused when q != nullptr): L[m,j] = W[ids[m,j]] . h[m]; q = softmax.
 // `tickets` (M ints, zero on entry, left zero on exit) enable the fusion.
+// span > 0: warps take the candidates in blocks of `span` columns (all rows
+// of a block together) instead of row by row; see the kernel.
 cudaError_t launch_gather_logits(const bf16_t* W, const bf16_t* h, const int32_t* ids, int64_t n,
                                  int d, int M, int K, float* logits, float* q, float inv_temp,
-                                 int* tickets, int* err, cudaStream_t s);
+                                 int* tickets, int* err, cudaStream_t s, int span = 0);
 
 // K6 standalone: row softmax of an M x K matrix (any K).
 cudaError_t launch_row_softmax(const float* L, int M, int64_t K, float inv_temp, float* q,
                                cudaStream_t s);
 
-// K7: dense logits over all rows of W (n x d).
-cudaError_t launch_dense_logits(const bf16_t* W, const bf16_t* h, int64_t n, int d, int M,
-                                float* logits, cudaStream_t s);
+// Tensor-core row products (rows_tc.cu): out[m * ldo + j] = X[j] . Y[m] for
+// every row j of X (n x kdim) and hidden vector m of Y (M x kdim); any M
+// (blocks of kRowsTcMaxN). Used for the dense and pruned heads and the
+// global path's score writeback.
+constexpr int kRowsTcMaxN = 256;
+cudaError_t launch_rows_dense_tc(const bf16_t* X, int64_t n, int kdim, const bf16_t* Y, int M,
+                                 float* out, int64_t ldo, int* err, cudaStream_t s);
 
 int* device_error_word();  // this device's error word (nullptr on failure)
 

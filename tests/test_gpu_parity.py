@@ -169,7 +169,7 @@ def test_gather_logits_and_bad_id(L, small):
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("K", [1, 5, 1002, 70000])
+@pytest.mark.parametrize("K", [1, 5, 1002, 70000, 200000, 300000])
 @pytest.mark.parametrize("temp", [1.0, 3.0])
 def test_candidate_softmax(L, K, temp):
     import torch
@@ -222,3 +222,38 @@ def test_host_validation_errors(L, small):
     with pytest.raises(L.LmheadError) as e:
         L.two_stage(L.GLOBAL, W, A, B, h, tok, 64, workspace=tiny)
     assert e.value.status == -4
+
+
+# Local mode at larger M: the gather takes the candidates in blocks of 16
+# tiles (ragged last block when the tile count is not a multiple of 16);
+# tiles of a multiple of 128 rows and not, d not a multiple of 64, M above
+# one 128-row TMEM block of the scoring kernel, k_tile up to 8.
+@pytest.mark.parametrize("M", [16, 33, 150])
+@pytest.mark.parametrize("T,k", [(128, 2), (256, 4), (64, 8), (100, 3), (7, 3)])
+def test_two_stage_larger_m(L, M, T, k):
+    case = make_case(1500, 200, 24, M, seed=17, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    ids, lg, q = L.two_stage(L.LOCAL, W, A, B, h, tok, T, k, temperature=0.7)
+    _, S, h64, SL = oracle_scores(case, with_slack=True)
+    ids = host(ids)
+    P.check_ids("local", ids, S, case["tok"], T, k, slack_pos=SL)
+    ex = P.exact_logits(case["W"], h64, ids)
+    P.check_logits(host(lg), ex)
+    P.check_q(host(q), ex, 0.7)
+    assert L.last_device_error() == 0
+
+
+@pytest.mark.parametrize("M", [1, 17, 300])
+def test_dense_head_blocks(L, M):
+    # CUDA cores at M = 1; tensor cores above, M > 256 in blocks of 256 hidden
+    # vectors; n not a multiple of 128
+    case = make_case(1000, 96, 16, M, seed=18, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    lg, q = L.dense_head(W, h)
+    h64 = O.bf16_bits_to_f64(case["h"])
+    Z = O.dense_logits(O.bf16_bits_to_f64(case["W"]), h64)
+    P.check_logits(host(lg), Z)
+    qq = host(q)
+    for m in (0, M // 2, M - 1):
+        assert np.abs(qq[m] - O.candidate_softmax(Z[m])).max() < P.Q_ABS
+    assert L.last_device_error() == 0
