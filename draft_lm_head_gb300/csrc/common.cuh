@@ -124,6 +124,18 @@ inline cudaError_t launch_kernel(bool pdl, void (*kernel)(KArgs...), dim3 grid, 
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// CTA-wide barriers that count arriving threads one by one (PTX
+// barrier.sync without .aligned), so they are correct when the lanes of a
+// warp arrive at different times, as in the warp-specialised kernels where
+// lane 0 runs a role loop while lanes 1-31 go straight to the final barrier.
+// A globaltimer trace of the fused scoring kernel showed __syncthreads (the
+// aligned form) releasing such a CTA before its epilogue warps had arrived.
+__device__ __forceinline__ void cta_sync() { asm volatile("barrier.sync 0;" ::: "memory"); }
+// Named barrier `id` over `count` threads (a multiple of 32), same counting.
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -40,28 +40,20 @@ __device__ __forceinline__ void warp_row_softmax(const float* L, float* q, int K
   for (int j = lane; j < K; j += 32) q[j] = __expf(__ldcg(L + j) * inv_temp - gmx) * inv;
 }
 
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
-gather_logits_kernel(const bf16_t* __restrict__ W, const bf16_t* __restrict__ h,
-                     const int32_t* __restrict__ ids, int64_t n, int d, int M, int K,
-                     int span, float* __restrict__ logits, float* __restrict__ q,
-                     float inv_temp, int* __restrict__ tickets, int* __restrict__ err) {
-  const int lane = threadIdx.x & 31;
-  const int64_t c = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  pdl_trigger();
-  pdl_wait();  // ids come from the previous kernel
-  if (c >= (int64_t)M * K) return;
-  // warp c -> candidate (m, j). Row-major, or by blocks of `span` columns:
-  // every row's candidates of one block are taken together, so a W row that
-  // several rows picked is requested several times within a short window
-  // (the repeats hit L2), while consecutive warps still share h[m] (L1).
-  int m;
-  int64_t flat = c;
+// warp c -> candidate (m, j), returned as the flat index m * K + j.
+// Row-major, or by blocks of `span` columns: every row's candidates of one
+// block are taken together, so a W row that several rows picked is requested
+// several times within a short window (the repeats hit L2), while consecutive
+// warps still share h[m].
+// (M * K < 2^31 is checked on the host, so 32-bit arithmetic suffices.)
+__device__ __forceinline__ uint32_t candidate_of(uint32_t c, uint32_t M, uint32_t K, uint32_t span,
+                                                 int* m_out) {
   if (span > 0 && span < K) {
-    const int64_t full = K / span, cut = full * (int64_t)M * span;
-    int64_t j0, w, r;
+    const uint32_t full = K / span, cut = full * M * span;
+    uint32_t j0, w, r;
     if (c < cut) {
-      const int64_t b = c / ((int64_t)M * span);
-      r = c - b * (int64_t)M * span;
+      const uint32_t b = c / (M * span);
+      r = c - b * M * span;
       j0 = b * span;
       w = span;
     } else {
@@ -69,11 +61,50 @@ gather_logits_kernel(const bf16_t* __restrict__ W, const bf16_t* __restrict__ h,
       j0 = full * span;
       w = K - j0;
     }
-    m = (int)(r / w);
-    flat = (int64_t)m * K + j0 + (r - (int64_t)m * w);
-  } else {
-    m = (int)(c / K);
+    const uint32_t m = r / w;
+    *m_out = (int)m;
+    return m * K + j0 + (r - m * w);
   }
+  *m_out = (int)(c / K);
+  return c;
+}
+
+// WPC warps per CTA, UNR 16-byte loads of W in flight per lane, at least
+// MINB CTAs per SM. When SH and all warps of the CTA share one hidden vector,
+// h[m] is staged in shared memory once (before waiting for the ids: h is an
+// input), so only the W row streams through L1 per candidate. Measured on the
+// n=128256, d=4096, M=64 workload: 8 warps, 4 loads, 6 CTAs per SM (48 warps)
+// with staging is the fastest of the shapes tried (4-16 warps, 2-16 loads).
+template <int WPC, int UNR, int MINB, bool SH>
+__global__ void __launch_bounds__(WPC * 32, MINB)
+gather_logits_kernel(const bf16_t* __restrict__ W, const bf16_t* __restrict__ h,
+                     const int32_t* __restrict__ ids, int64_t n, int d, int M, int K,
+                     int span, float* __restrict__ logits, float* __restrict__ q,
+                     float inv_temp, int* __restrict__ tickets, int* __restrict__ err) {
+  extern __shared__ uint4 h_s[];
+  const int lane = threadIdx.x & 31;
+  const uint32_t MK = (uint32_t)M * (uint32_t)K;
+  const uint32_t c = blockIdx.x * WPC + (threadIdx.x >> 5);
+  const int nvec = d >> 3;
+  pdl_trigger();
+  bool staged = false;
+  if (SH) {
+    const uint32_t cb = blockIdx.x * WPC;
+    const uint32_t ce = cb + WPC - 1 < MK ? cb + WPC - 1 : MK - 1;
+    int mb, me;
+    candidate_of(cb, M, K, span, &mb);
+    candidate_of(ce, M, K, span, &me);
+    staged = mb == me;  // the same for every thread of the CTA
+    if (staged) {
+      const uint4* hrow = reinterpret_cast<const uint4*>(h + (size_t)mb * d);
+      for (int v = threadIdx.x; v < nvec; v += WPC * 32) h_s[v] = __ldg(hrow + v);
+      cta_sync();
+    }
+  }
+  pdl_wait();  // ids come from the previous kernel
+  if (c >= MK) return;
+  int m;
+  const uint32_t flat = candidate_of(c, M, K, span, &m);
   const int32_t id = __ldg(ids + flat);
   float s;
   if (id < 0 || (int64_t)id >= n) {
@@ -82,10 +113,14 @@ gather_logits_kernel(const bf16_t* __restrict__ W, const bf16_t* __restrict__ h,
   } else {
     const uint4* wrow = reinterpret_cast<const uint4*>(W + (size_t)id * d);
     const uint4* hrow = reinterpret_cast<const uint4*>(h + (size_t)m * d);
-    const int nvec = d >> 3;
     float acc = 0.f;
-#pragma unroll 4
-    for (int v = lane; v < nvec; v += 32) acc += dot8(ldg_nc_v4(wrow + v), __ldg(hrow + v));
+    if (staged) {
+#pragma unroll UNR
+      for (int v = lane; v < nvec; v += 32) acc += dot8(ldg_nc_v4(wrow + v), h_s[v]);
+    } else {
+#pragma unroll UNR
+      for (int v = lane; v < nvec; v += 32) acc += dot8(ldg_nc_v4(wrow + v), __ldg(hrow + v));
+    }
     s = warp_sum(acc);
   }
   if (lane == 0) logits[flat] = s;
@@ -134,16 +169,16 @@ row_softmax_cluster_kernel(const float* __restrict__ L, int64_t K, float inv_tem
   }
   mx = warp_max(mx);
   if (lane == 0) red[warp] = mx;
-  __syncthreads();
+  cta_sync();
   float bm = red[0];
   for (int w = 1; w < kWarps; ++w) bm = fmaxf(bm, red[w]);
-  __syncthreads();  // red is reused below
+  cta_sync();  // red is reused below
   float sum = 0.f;
 #pragma unroll
   for (int e = 0; e < EPT; ++e) sum += bm == -INFINITY ? 0.f : __expf(z[e] - bm);
   sum = warp_sum(sum);
   if (lane == 0) red[warp] = sum;
-  __syncthreads();
+  cta_sync();
   if (tid == 0) {
     float bs = 0.f;
     for (int w = 0; w < kWarps; ++w) bs += red[w];
@@ -194,13 +229,13 @@ row_softmax_kernel(const float* __restrict__ L, int64_t K, float inv_temp, float
   float ws = (mx == -INFINITY) ? 0.f : sum * __expf(mx - wm);
   ws = warp_sum(ws);
   if (lane == 0) { red_m[warp] = wm; red_s[warp] = ws; }
-  __syncthreads();
+  cta_sync();
   float gm = red_m[0];
   for (int w = 1; w < 8; ++w) gm = fmaxf(gm, red_m[w]);
   float gs = 0.f;
   for (int w = 0; w < 8; ++w) gs += (red_m[w] == -INFINITY) ? 0.f : red_s[w] * __expf(red_m[w] - gm);
   const float inv = 1.f / gs;
-  __syncthreads();  // q may alias L: every read of the row is done
+  cta_sync();  // q may alias L: every read of the row is done
   for (int64_t j = tid; j < K; j += blockDim.x) qrow[j] = __expf(row[j] * inv_temp - gm) * inv;
 }
 
@@ -224,11 +259,11 @@ row_softmax_reg_kernel(const float* __restrict__ L, int K, float inv_temp, float
   }
   mx = warp_max(mx);
   if (lane == 0) red[warp] = mx;
-  __syncthreads();
+  cta_sync();
   float gm = red[0];
 #pragma unroll
   for (int w = 1; w < 8; ++w) gm = fmaxf(gm, red[w]);
-  __syncthreads();  // red is reused below
+  cta_sync();  // red is reused below
   float sum = 0.f;
 #pragma unroll
   for (int e = 0; e < EPT; ++e) {
@@ -237,7 +272,7 @@ row_softmax_reg_kernel(const float* __restrict__ L, int K, float inv_temp, float
   }
   sum = warp_sum(sum);
   if (lane == 0) red[warp] = sum;
-  __syncthreads();
+  cta_sync();
   float gs = 0.f;
 #pragma unroll
   for (int w = 0; w < 8; ++w) gs += red[w];
@@ -251,15 +286,29 @@ row_softmax_reg_kernel(const float* __restrict__ L, int K, float inv_temp, float
 
 }  // namespace
 
+template <int WPC, int UNR, int MINB, bool SH>
+cudaError_t launch_gather_v(const bf16_t* W, const bf16_t* h, const int32_t* ids, int64_t n, int d,
+                            int M, int K, float* logits, float* q, float inv_temp, int* tickets,
+                            int* err, cudaStream_t s, int span) {
+  const int64_t total = (int64_t)M * K;
+  const unsigned grid = (unsigned)((total + WPC - 1) / WPC);
+  const size_t smem = SH ? (size_t)d * 2 : 0;
+  static int smem_set[64] = {0};
+  if (SH) {
+    cudaError_t e = ensure_dynamic_smem(gather_logits_kernel<WPC, UNR, MINB, SH>, smem, smem_set);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_kernel(true, gather_logits_kernel<WPC, UNR, MINB, SH>, dim3(grid),
+                       dim3(WPC * 32), smem, s, W, h, ids, n, d, M, K, span, logits, q,
+                       inv_temp, tickets, err);
+}
+
 cudaError_t launch_gather_logits(const bf16_t* W, const bf16_t* h, const int32_t* ids, int64_t n,
                                  int d, int M, int K, float* logits, float* q, float inv_temp,
                                  int* tickets, int* err, cudaStream_t s, int span) {
-  const int64_t total = (int64_t)M * K;
-  const unsigned grid = (unsigned)((total + kWarpsPerCta - 1) / kWarpsPerCta);
-  return launch_kernel(true, gather_logits_kernel, dim3(grid), dim3(kWarpsPerCta * 32), 0, s, W, h,
-                       ids, n, d, M, K, span, logits, q, inv_temp, tickets, err);
+  return launch_gather_v<kWarpsPerCta, 4, 6, true>(W, h, ids, n, d, M, K, logits, q, inv_temp,
+                                                     tickets, err, s, span);
 }
-
 
 cudaError_t launch_row_softmax(const float* L, int M, int64_t K, float inv_temp, float* q,
                                cudaStream_t s) {

@@ -38,13 +38,13 @@ __global__ void __launch_bounds__(256) project_u_kernel(const bf16_t* __restrict
   const uint4* brow = reinterpret_cast<const uint4*>(B + (size_t)min(k, r - 1) * d);
   for (int c0 = 0; c0 < d; c0 += kDChunk) {
     const int nvec = min(kDChunk, d - c0) / 8;
-    __syncthreads();
+    cta_sync();
     for (int i = threadIdx.x; i < mb * nvec; i += blockDim.x) {
       const int mm = i / nvec, v = i - mm * nvec;
       hs[mm * (kDChunk / 8) + v] =
           *reinterpret_cast<const uint4*>(h + (size_t)(m0 + mm) * d + c0 + v * 8);
     }
-    __syncthreads();
+    cta_sync();
     if (k < r) {
 #pragma unroll 2
       for (int v = lane; v < nvec; v += 32) {
@@ -121,7 +121,7 @@ project_u_tc_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_const
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
-  __syncthreads();
+  cta_sync();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
 
@@ -244,7 +244,7 @@ project_u_gemv_kernel(const bf16_t* __restrict__ B, const bf16_t* __restrict__ h
       if (lane == 0) red[mm][warp] = acc;
     }
   }
-  __syncthreads();
+  cta_sync();
   if (tid < M) {
     float s = 0.f;
 #pragma unroll

@@ -98,7 +98,7 @@ rows_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
-  __syncthreads();
+  cta_sync();
   tc::fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
 
@@ -227,7 +227,7 @@ rows_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
   }
 
   tc::fence_before_sync();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 2 * p.acc_cols);

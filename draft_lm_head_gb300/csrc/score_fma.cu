@@ -96,12 +96,12 @@ local_topk_fma_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u
 
   for (int64_t p0 = t0; p0 < t1; p0 += kChunk) {
     const int rows = (int)min((int64_t)kChunk, t1 - p0);
-    __syncthreads();  // us staged / previous chunk's selection done
+    cta_sync();  // us staged / previous chunk's selection done
     for (int j = threadIdx.x; j < rows; j += blockDim.x)
       sid[j] = token_ids ? token_ids[p0 + j] : (int32_t)(p0 + j);
     score_chunk(A, r, p0, rows, mb, us,
                 [&](int mm, int j, float s) { sc[mm][j] = s; });
-    __syncthreads();
+    cta_sync();
     if (warp < mb) {
       // new list = top-k_tile of (current list U this chunk)
       const int want = min(k_tile, lcount + rows);
@@ -166,7 +166,7 @@ score_all_fma_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u,
   const int64_t p0 = (int64_t)blockIdx.x * kChunk;
   const int rows = (int)min((int64_t)kChunk, n - p0);
   stage_u(u, r, m0, mb, us);
-  __syncthreads();
+  cta_sync();
   score_chunk(A, r, p0, rows, mb, us, [&](int mm, int j, float s) {
     S[(size_t)(m0 + mm) * n + p0 + j] = s;
   });

@@ -201,7 +201,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
-  __syncthreads();
+  cta_sync();
   tc::fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
 
@@ -370,7 +370,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
 #pragma unroll
           for (int j = 0; j < KT; ++j)
             xchg[ml * KT + j] = make_float2(Lst.s[j], __int_as_float(Lst.k[j]));
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+          named_sync(1, 128);
           if (rep == 0) {
             for (int r2 = 1; r2 < p.R; ++r2) {
               const int ol = (q + r2 * qstep) * 32 + lane;
@@ -389,7 +389,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
                              Lst, true);
             }
           }
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+          named_sync(1, 128);
 #pragma unroll
           for (int j = 0; j < kSub; ++j) sub[j].reset();
         }
@@ -473,7 +473,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       }
     }
     __threadfence();
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    named_sync(1, 128);
     if (warp == 2 && lane == 0) {
       const bool go = !(*abort_flag);
       for (int side = 0; side < 2; ++side) {
@@ -488,7 +488,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
         ctl.decision[side] = (old == parts - 1) ? 1 : 0;
       }
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    named_sync(1, 128);
     for (int side = 0; side < 2; ++side) {
       if (!ctl.decision[side]) continue;
       const int64_t t = part_tile[side];
@@ -520,7 +520,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
   }
 
   tc::fence_before_sync();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -542,7 +542,7 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "barrier.red.and.pred q, 1, 128, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"((uint32_t)v)
@@ -590,7 +590,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
-  __syncthreads();
+  cta_sync();
   tc::fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
 
@@ -601,7 +601,18 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
       tc::prefetch_tmap(&umap);
       uint32_t it = 0;  // stage sequence
       int c = 0;        // chunk sequence
+      const int grp = min(min(4, NS), kblocks);
       bool ok = true, u_loaded = false;
+      // u is written by the previous kernel: wait for it, then load it once
+      auto load_u = [&]() {
+        pdl_wait();
+        tc::mbar_arrive_expect_tx(&ctl.ufull, (uint32_t)(kblocks * kStageBytes));
+        for (int ub = 0; ub < kblocks; ++ub)
+          for (int rep = 0; rep < p.R; ++rep)
+            tc::tma_load_2d(u_s + (size_t)ub * kStageBytes + (size_t)rep * p.rows_per_rep * 128,
+                            &umap, &ctl.ufull, ub * kKBlock, y * p.rows_per_rep - p.lane_shift);
+        u_loaded = true;
+      };
       int64_t tile = blockIdx.x < p.tiles ? (int64_t)blockIdx.x : -1;
       int64_t next = -1;
       while (ok) {
@@ -627,37 +638,37 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
           const bool last = j == cpt - 1 || (gc + 1) * kChunk >= n;
           desc_tile[c % kDescRing] = (int)tile;
           desc_chunk[c % kDescRing] = j | (last ? (int)0x80000000 : 0);
-          for (int kb = 0; kb < kblocks; ++kb, ++it) {
-            const int s = (int)(it % NS);
-            if (it >= (uint32_t)NS && !tc::mbar_wait(&ctl.empty[s], ((it / NS) & 1) ^ 1, abort_flag)) {
-              ok = false;
-              break;
+          // a group of up to four boxes (one chunk at r = 256) is issued back to
+          // back once all its stages are free, so each row's 128-byte pieces
+          // are requested together (contiguous DRAM reads); one box at a time,
+          // the requests scatter and the stream loses a third of its rate
+          for (int kb0 = 0; kb0 < kblocks && ok; kb0 += grp) {
+            const int gcount = min(grp, kblocks - kb0);
+            // stages of the group that are still in use free up only once the
+            // MMA runs, which needs u: load it before waiting on them
+            if (!u_loaded && it + (uint32_t)gcount > (uint32_t)NS) load_u();
+            for (int g2 = 0; g2 < gcount; ++g2) {
+              const uint32_t itg = it + (uint32_t)g2;
+              if (itg >= (uint32_t)NS &&
+                  !tc::mbar_wait(&ctl.empty[itg % NS], ((itg / NS) & 1) ^ 1, abort_flag)) {
+                ok = false;
+                break;
+              }
             }
-            tc::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
-            tc::tma_load_2d(stage_s + (size_t)s * kStageBytes, &amap, &ctl.full[s], kb * kKBlock,
-                            (int)(gc * kChunk));
-            if (!u_loaded && (it + 1 >= (uint32_t)NS || (j == cpt - 1 && kb == kblocks - 1))) {
-              // ring filled (or first tile issued): now wait for u, written by the previous kernel
-              pdl_wait();
-              tc::mbar_arrive_expect_tx(&ctl.ufull, (uint32_t)(kblocks * kStageBytes));
-              for (int ub = 0; ub < kblocks; ++ub)
-                for (int rep = 0; rep < p.R; ++rep)
-                  tc::tma_load_2d(u_s + (size_t)ub * kStageBytes + (size_t)rep * p.rows_per_rep * 128,
-                                  &umap, &ctl.ufull, ub * kKBlock, y * p.rows_per_rep - p.lane_shift);
-              u_loaded = true;
+            if (!ok) break;
+            for (int g2 = 0; g2 < gcount; ++g2, ++it) {
+              const int s = (int)(it % NS);
+              tc::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
+              tc::tma_load_2d(stage_s + (size_t)s * kStageBytes, &amap, &ctl.full[s],
+                              (kb0 + g2) * kKBlock, (int)(gc * kChunk));
             }
+            // ring filled, or the first tile fully issued: u next
+            if (!u_loaded && (it >= (uint32_t)NS || (j == cpt - 1 && kb0 + gcount == kblocks)))
+              load_u();
           }
           ++c;
         }
-        if (!u_loaded) {  // no tile at all for this CTA
-          pdl_wait();
-          tc::mbar_arrive_expect_tx(&ctl.ufull, (uint32_t)(kblocks * kStageBytes));
-          for (int ub = 0; ub < kblocks; ++ub)
-            for (int rep = 0; rep < p.R; ++rep)
-              tc::tma_load_2d(u_s + (size_t)ub * kStageBytes + (size_t)rep * p.rows_per_rep * 128,
-                              &umap, &ctl.ufull, ub * kKBlock, y * p.rows_per_rep - p.lane_shift);
-          u_loaded = true;
-        }
+        if (!u_loaded) load_u();  // no tile at all for this CTA
         if (tile >= 0 && next < 0) next = (int64_t)p.G + atomicAdd(counter, 1);
         tile = next;
         next = -1;
@@ -786,7 +797,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
 #pragma unroll
           for (int jj = 0; jj < KT; ++jj)
             xchg[ml * KT + jj] = make_float2(Lst.s[jj], __int_as_float(Lst.k[jj]));
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+          named_sync(1, 128);
           if (rep == 0) {
             for (int r2 = 1; r2 < p.R; ++r2) {
               const int ol = (q + r2 * qstep) * 32 + lane;
@@ -797,7 +808,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
               }
             }
           }
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+          named_sync(1, 128);
         }
         if (valid_out)
           write_tile<KT>(p, m, tile, (int)min((int64_t)KT, min(n, (int64_t)(tile + 1) * T) - (int64_t)tile * T),
@@ -809,7 +820,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
   }
 
   tc::fence_before_sync();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);

@@ -45,7 +45,7 @@ __device__ void bitonic_desc(uint64_t* keys, int P) {
           keys[par] = a;
         }
       }
-      __syncthreads();
+      cta_sync();
     }
   }
 }
@@ -80,7 +80,7 @@ segment_topk_kernel(const float* __restrict__ S, const int32_t* __restrict__ tok
   if (len <= 2 * kCap) {
     const int P = pow2_at_least(len);
     for (int i = tid; i < P; i += blockDim.x) keys[i] = i < len ? key_at(row, token_ids, p0 + i) : 0ull;
-    __syncthreads();
+    cta_sync();
     bitonic_desc(keys, P);
     for (int j = tid; j < kk; j += blockDim.x) {
       out_ids[obase + j] = key_id(keys[j]);
@@ -93,22 +93,22 @@ segment_topk_kernel(const float* __restrict__ S, const int32_t* __restrict__ tok
   int gt = 0;  // keys above hi (all selected)
   for (int shift = 64 - kDigit;; shift = shift >= kDigit ? shift - kDigit : 0) {
     for (int i = tid; i < kBins; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
+    cta_sync();
     for (int64_t p = p0 + tid; p < p1; p += blockDim.x) {
       const uint64_t key = key_at(row, token_ids, p);
       if (key >= lo && key <= hi) atomicAdd(&hist[(key >> shift) & (kBins - 1)], 1u);
     }
-    __syncthreads();
+    cta_sync();
     // suffix sums over threads' groups of 4 bins (bins descending = keys descending)
     const int g = kThreads - 1 - tid;  // thread tid owns bins [4g, 4g+4)
     uint32_t local = hist[4 * g] + hist[4 * g + 1] + hist[4 * g + 2] + hist[4 * g + 3];
     part[tid] = local;
-    __syncthreads();
+    cta_sync();
     for (int off = 1; off < kThreads; off <<= 1) {
       const uint32_t v = tid >= off ? part[tid - off] : 0u;
-      __syncthreads();
+      cta_sync();
       part[tid] += v;
-      __syncthreads();
+      cta_sync();
     }
     // part[tid] = keys in bins >= 4g (inclusive); above = keys in bins >= 4g+4
     uint32_t above = part[tid] - local;
@@ -127,17 +127,17 @@ segment_topk_kernel(const float* __restrict__ S, const int32_t* __restrict__ tok
         above += hist[b];
       }
     }
-    __syncthreads();
+    cta_sync();
     lo = s_lo;
     hi = s_hi;
     gt = s_gt;
     const int bin_count = s_bin_count;
-    __syncthreads();
+    cta_sync();
     if (bin_count <= kCap || shift == 0) break;
   }
 
   if (tid == 0) { s_sel = 0; s_cand = 0; }
-  __syncthreads();
+  cta_sync();
   for (int64_t p = p0 + tid; p < p1; p += blockDim.x) {
     const uint64_t key = key_at(row, token_ids, p);
     if (key > hi) {
@@ -147,17 +147,17 @@ segment_topk_kernel(const float* __restrict__ S, const int32_t* __restrict__ tok
       if (c < kCap) keys[kCap + c] = key;
     }
   }
-  __syncthreads();
+  cta_sync();
   const int ncand = min(s_cand, kCap);
   const int P = pow2_at_least(ncand);
   for (int i = ncand + tid; i < P; i += blockDim.x) keys[kCap + i] = 0ull;
-  __syncthreads();
+  cta_sync();
   bitonic_desc(keys + kCap, P);
   const int take = kk - gt;
   for (int i = tid; i < take; i += blockDim.x) keys[gt + i] = keys[kCap + i];
   const int Ps = pow2_at_least(kk);
   for (int i = kk + tid; i < Ps; i += blockDim.x) keys[i] = 0ull;
-  __syncthreads();
+  cta_sync();
   bitonic_desc(keys, Ps);
   for (int j = tid; j < kk; j += blockDim.x) {
     out_ids[obase + j] = key_id(keys[j]);
