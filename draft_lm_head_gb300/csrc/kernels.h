@@ -39,10 +39,6 @@ cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t
                                  float* out_scores, void* partials, int* tile_tickets, int* err,
                                  cudaStream_t s);
 
-// K2 (CUDA cores): S[m, p] = A[p] . u[m] for every position p, fp32 to HBM.
-cudaError_t launch_score_all_fma(const bf16_t* A, const bf16_t* u, int64_t n, int r, int M,
-                                 float* S, cudaStream_t s);
-
 // K3: per row m, per segment of `seg_len` positions, exact top-k of S by
 // (score desc, vocabulary id asc). k <= kSelectMaxK.
 cudaError_t launch_segment_topk(const float* S, const int32_t* token_ids, int64_t n, int M,

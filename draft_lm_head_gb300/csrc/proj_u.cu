@@ -258,14 +258,15 @@ project_u_gemv_kernel(const bf16_t* __restrict__ B, const bf16_t* __restrict__ h
 
 cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int M, bf16_t* u,
                              int* zero_ptr, int zero_ints, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
   if (M <= kGemvMaxM && d <= 8192) {
     const int vpt = (d + 1023) / 1024;
-    if (vpt <= 1) project_u_gemv_kernel<1, 8><<<r, kGemvThreads, 0, s>>>(B, h, d, r, M, u, zero_ptr, zero_ints);
-    else if (vpt <= 2) project_u_gemv_kernel<2, 8><<<r, kGemvThreads, 0, s>>>(B, h, d, r, M, u, zero_ptr, zero_ints);
-    else if (vpt <= 4) project_u_gemv_kernel<4, 8><<<r, kGemvThreads, 0, s>>>(B, h, d, r, M, u, zero_ptr, zero_ints);
-    else if (M <= 4) project_u_gemv_kernel<8, 4><<<r, kGemvThreads, 0, s>>>(B, h, d, r, M, u, zero_ptr, zero_ints);
+    if (vpt <= 1) e = launch_kernel(false, project_u_gemv_kernel<1, 8>, dim3(r), dim3(kGemvThreads), 0, s, B, h, d, r, M, u, zero_ptr, zero_ints);
+    else if (vpt <= 2) e = launch_kernel(false, project_u_gemv_kernel<2, 8>, dim3(r), dim3(kGemvThreads), 0, s, B, h, d, r, M, u, zero_ptr, zero_ints);
+    else if (vpt <= 4) e = launch_kernel(false, project_u_gemv_kernel<4, 8>, dim3(r), dim3(kGemvThreads), 0, s, B, h, d, r, M, u, zero_ptr, zero_ints);
+    else if (M <= 4) e = launch_kernel(false, project_u_gemv_kernel<8, 4>, dim3(r), dim3(kGemvThreads), 0, s, B, h, d, r, M, u, zero_ptr, zero_ints);
     else goto tensor_cores;
-    return cudaGetLastError();
+    return e;
   }
 tensor_cores:
   if (d <= kProjTcMaxD) {
@@ -279,7 +280,7 @@ tensor_cores:
         !make_bf16_map(&bmap, B, (uint64_t)r, (uint64_t)d, kTcN, 64))
       return cudaErrorInvalidValue;
     static int smem_set[64] = {0};
-    cudaError_t e = ensure_dynamic_smem(project_u_tc_kernel, smem, smem_set);
+    e = ensure_dynamic_smem(project_u_tc_kernel, smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(KS, (r + kTcN - 1) / kTcN, (M + kTcHid - 1) / kTcHid);
@@ -297,8 +298,8 @@ tensor_cores:
                               zero_ints, device_error_word());
   }
   dim3 grid((r + kRowsPerCta - 1) / kRowsPerCta, (M + kMB - 1) / kMB);
-  project_u_kernel<<<grid, 256, 0, s>>>(B, h, d, r, M, u, zero_ptr, zero_ints);
-  return cudaGetLastError();
+  return launch_kernel(false, project_u_kernel, grid, dim3(256), 0, s, B, h, d, r, M, u, zero_ptr,
+                       zero_ints);
 }
 
 }  // namespace lmhead

@@ -1,8 +1,8 @@
 // Stage-1 scoring on CUDA cores (EAGLE-4 notes, "A Local Top-k based
-// variant"): scores = A u over vocabulary rows, either
-//   K4 fused: kept on chip per vocabulary tile, reduced to the tile's top
-//             k_tile and written out through token_ids (no score writeback);
-//   K2:       written to HBM for the global Top-k (the "original flow").
+// variant"): scores = A u over the vocabulary rows of a tile, kept on chip,
+// reduced to the tile's top k_tile and written out through token_ids (no
+// score writeback). It serves the tile shapes the tensor-core kernel does not
+// (tiles under 32 rows, k_tile not in {1, 2, 4, 8}, r > 512).
 //
 // This is the small-batch engine: A is read once with 16-byte loads, one warp
 // per row with the rank dimension split across lanes; u (M x r) sits in
@@ -155,23 +155,6 @@ local_topk_fma_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u
   }
 }
 
-// ---------------------------------------------------------------- K2 (fma)
-// grid: (ceil(n / kChunk), ceil(M / kMB)).
-__global__ void __launch_bounds__(kThreads)
-score_all_fma_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u, int64_t n,
-                     int r, int M, float* __restrict__ S) {
-  extern __shared__ float us[];
-  const int m0 = blockIdx.y * kMB;
-  const int mb = min(kMB, M - m0);
-  const int64_t p0 = (int64_t)blockIdx.x * kChunk;
-  const int rows = (int)min((int64_t)kChunk, n - p0);
-  stage_u(u, r, m0, mb, us);
-  cta_sync();
-  score_chunk(A, r, p0, rows, mb, us, [&](int mm, int j, float s) {
-    S[(size_t)(m0 + mm) * n + p0 + j] = s;
-  });
-}
-
 }  // namespace
 
 cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
@@ -187,22 +170,8 @@ cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_
     if (e != cudaSuccess) return e;
   }
   dim3 grid((unsigned)tiles, (M + kMB - 1) / kMB);
-  local_topk_fma_kernel<<<grid, kThreads, smem, s>>>(A, u, token_ids, n, r, M, T, k_tile, K,
-                                                     out_ids, out_scores);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_score_all_fma(const bf16_t* A, const bf16_t* u, int64_t n, int r, int M,
-                                 float* S, cudaStream_t s) {
-  const size_t smem = (size_t)kMB * r * sizeof(float);
-  if (smem > 48 * 1024) {
-    static int smem_set[64] = {0};
-    cudaError_t e = ensure_dynamic_smem(score_all_fma_kernel, smem, smem_set);
-    if (e != cudaSuccess) return e;
-  }
-  dim3 grid((unsigned)((n + kChunk - 1) / kChunk), (M + kMB - 1) / kMB);
-  score_all_fma_kernel<<<grid, kThreads, smem, s>>>(A, u, n, r, M, S);
-  return cudaGetLastError();
+  return launch_kernel(false, local_topk_fma_kernel, grid, dim3(kThreads), smem, s, A, u, token_ids,
+                       n, r, M, T, k_tile, K, out_ids, out_scores);
 }
 
 }  // namespace lmhead

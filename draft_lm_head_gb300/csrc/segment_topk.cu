@@ -179,9 +179,8 @@ cudaError_t launch_segment_topk(const float* S, const int32_t* token_ids, int64_
   cudaError_t e = ensure_dynamic_smem(segment_topk_kernel, smem, smem_set);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)segs, M);
-  segment_topk_kernel<<<grid, kThreads, smem, s>>>(S, token_ids, n, seg_len, k, K, out_ids,
-                                                   out_scores);
-  return cudaGetLastError();
+  return launch_kernel(false, segment_topk_kernel, grid, dim3(kThreads), smem, s, S, token_ids, n,
+                       seg_len, k, K, out_ids, out_scores);
 }
 
 }  // namespace lmhead
