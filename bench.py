@@ -200,6 +200,23 @@ def make_graph(torch, fn):
     return g
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x (a timing in ms); x itself when alone."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(world, rows_per_rank, steps, ms):
+    """Whole-job hidden vectors/s: every rank's rows of every step over the
+    slowest rank's time."""
+    return world * rows_per_rank * steps / (ms / 1e3)
+
+
 def run_ours(args):
     import ctypes
     global NROT
@@ -276,12 +293,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * M * args.steps / (ms / 1e3)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
+    value = aggregate_rate(world, M, args.steps, ms)
     launches = nl * args.steps
 
     # per-kernel durations: the profiled entry point records an event after every launch
@@ -354,12 +367,8 @@ def run_ours(args):
         e2e_step(i)
     e1.record()
     torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
-    e2e = {"value": round(world * M * args.steps / (ms_e2e / 1e3), 1), "unit": "hidden vecs/s",
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
+    e2e = {"value": round(aggregate_rate(world, M, args.steps, ms_e2e), 1), "unit": "hidden vecs/s",
            "h2d_bytes_per_step": int(hb.nbytes),
            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs[0]))}
 
