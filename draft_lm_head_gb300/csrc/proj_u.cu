@@ -76,20 +76,23 @@ __global__ void __launch_bounds__(256) project_u_kernel(const bf16_t* __restrict
 
 
 // ---------------------------------------------------------------- tensor cores
-// u tile (128 hidden rows x 32 rows of B) = h_tile . B_tile^T, split over d
-// across the KS CTAs of a thread-block cluster. Each CTA loads its d-slice of
-// h (zero-filled past M and d) and of B by TMA, runs the MMAs into TMEM,
-// parks its fp32 partial in shared memory, and after a cluster barrier the
-// CTAs reduce the partials through distributed shared memory in a fixed
-// rank order (deterministic), round to bf16 and store u.
+// u tile (up to 128 hidden rows x NB rows of B) = h_tile . B_tile^T, split
+// over d across the KS CTAs of a thread-block cluster. Each CTA loads its
+// d-slice of h (hrows = min(M, 128) rows; the MMA's other rows hold whatever
+// shared memory held, and their output lanes are never read) and of B by
+// TMA, runs the MMAs into TMEM, parks its fp32 partial in shared memory, and
+// after a cluster barrier the CTAs reduce the partials through distributed
+// shared memory in a fixed rank order (deterministic), round to bf16 and
+// store u. Every CTA moves kslice x (hrows + 32) bf16 through TMA; loading
+// only the M real rows of h (not 128) keeps the projection short.
 constexpr int kTcHid = 128;  // MMA M
-constexpr int kTcN = 32;     // rows of B per cluster (MMA N)
+constexpr int kTcN = 32;     // rows of B per CTA (MMA N); 16 measured slower (more clusters to place)
 constexpr int kRedPitch = 33;  // fp32 partial row pitch (bank-conflict padding)
 
 __global__ void __launch_bounds__(128, 1)
 project_u_tc_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_constant__ CUtensorMap bmap,
-                    int r, int M, int kslice, bf16_t* __restrict__ u, int* zero_ptr, int zero_ints,
-                    int* err) {
+                    int r, int M, int kslice, int hrows, bf16_t* __restrict__ u, int* zero_ptr,
+                    int zero_ints, int* err) {
   extern __shared__ uint8_t raw[];
   __shared__ uint64_t bar_load, bar_mma;
   __shared__ uint32_t tmem_base;
@@ -128,7 +131,7 @@ project_u_tc_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_const
   if (threadIdx.x == 0) {
     tc::prefetch_tmap(&hmap);
     tc::prefetch_tmap(&bmap);
-    tc::mbar_arrive_expect_tx(&bar_load, (uint32_t)nkb * (kTcHid + kTcN) * 128);
+    tc::mbar_arrive_expect_tx(&bar_load, (uint32_t)nkb * (hrows + kTcN) * 128);
     for (int kb = 0; kb < nkb; ++kb) {
       const int x = ks * kslice + kb * 64;
       tc::tma_load_2d(h_s + (size_t)kb * kTcHid * 128, &hmap, &bar_load, x, hc * kTcHid);
@@ -169,8 +172,8 @@ project_u_tc_kernel(const __grid_constant__ CUtensorMap hmap, const __grid_const
   tc::fence_before_sync();
   tc::cluster_sync();  // every CTA's partial is in its shared memory
   // this CTA reduces rows [r0, r1) of the 128 x 32 tile over the KS ranks
-  const int rows_per = (kTcHid + KS - 1) / KS;
-  const int r0 = ks * rows_per, r1 = min(kTcHid, r0 + rows_per);
+  const int rows_per = (hrows + KS - 1) / KS;
+  const int r0 = ks * rows_per, r1 = min(hrows, r0 + rows_per);
   const uint32_t red_addr = tc::smem_addr(red);
   for (int o = threadIdx.x; o < (r1 - r0) * kTcN; o += blockDim.x) {
     const int rr = r0 + o / kTcN, c = o % kTcN;
@@ -274,9 +277,10 @@ tensor_cores:
     const int KS = min(8, (d + 511) / 512);
     const int kslice = ((d + KS - 1) / KS + 63) / 64 * 64;
     const int nkb = kslice / 64;
+    const int hrows = M < kTcHid ? M : kTcHid;
     const size_t smem = 1024 + (size_t)nkb * (kTcHid + kTcN) * 128;
     CUtensorMap hmap, bmap;
-    if (!make_bf16_map(&hmap, h, (uint64_t)M, (uint64_t)d, kTcHid, 64) ||
+    if (!make_bf16_map(&hmap, h, (uint64_t)M, (uint64_t)d, (uint32_t)hrows, 64) ||
         !make_bf16_map(&bmap, B, (uint64_t)r, (uint64_t)d, kTcN, 64))
       return cudaErrorInvalidValue;
     static int smem_set[64] = {0};
@@ -294,8 +298,8 @@ tensor_cores:
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, project_u_tc_kernel, hmap, bmap, r, M, kslice, u, zero_ptr,
-                              zero_ints, device_error_word());
+    return cudaLaunchKernelEx(&cfg, project_u_tc_kernel, hmap, bmap, r, M, kslice, hrows, u,
+                              zero_ptr, zero_ints, device_error_word());
   }
   dim3 grid((r + kRowsPerCta - 1) / kRowsPerCta, (M + kMB - 1) / kMB);
   return launch_kernel(false, project_u_kernel, grid, dim3(256), 0, s, B, h, d, r, M, u, zero_ptr,
