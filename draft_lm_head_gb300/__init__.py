@@ -26,7 +26,7 @@ LOCAL = 1
 __all__ = [
     "GLOBAL", "LOCAL", "LmheadError", "candidate_count", "workspace_size", "project_u",
     "lowrank_score_topk", "gather_logits", "candidate_softmax", "two_stage", "dense_head",
-    "pruned_head", "last_device_error", "version", "Workspace",
+    "pruned_head", "draft_select", "verify_chain", "last_device_error", "version", "Workspace",
 ]
 
 _BF16_OK = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (
@@ -200,3 +200,45 @@ def pruned_head(W_pruned: torch.Tensor, h: torch.Tensor, temperature: float = 1.
 def last_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return int(load().lmhead_last_device_error(_stream_ptr(stream)))
+
+
+def draft_select(q: torch.Tensor, ids: torch.Tensor, k_sel: int,
+                 parent_value: Optional[torch.Tensor] = None,
+                 uniforms: Optional[torch.Tensor] = None, stream=None):
+    """EAGLE-2 expansion of each row of q: its k_sel most likely candidates with
+    their path values, and (given uniforms) one Gumbel-max draw. Returns
+    (top_ids, top_q, top_value, sample_id, sample_q); the last two are None
+    without uniforms."""
+    M, K = q.shape
+    dev = q.device
+    top_ids = torch.empty((M, k_sel), dtype=torch.int32, device=dev)
+    top_q = torch.empty((M, k_sel), dtype=torch.float32, device=dev)
+    top_value = torch.empty((M, k_sel), dtype=torch.float32, device=dev)
+    sid = torch.empty(M, dtype=torch.int32, device=dev) if uniforms is not None else None
+    sq = torch.empty(M, dtype=torch.float32, device=dev) if uniforms is not None else None
+    check(load().lmhead_draft_select(
+        _typed(q, torch.float32, "q"), _typed(ids, torch.int32, "ids"), M, K, k_sel,
+        _typed(parent_value, torch.float32, "parent_value"),
+        _typed(uniforms, torch.float32, "uniforms"), top_ids.data_ptr(), top_q.data_ptr(),
+        top_value.data_ptr(), _typed(sid, torch.int32, "sample_id"),
+        _typed(sq, torch.float32, "sample_q"), _stream_ptr(stream)), "draft_select")
+    return top_ids, top_q, top_value, sid, sq
+
+
+def verify_chain(p: torch.Tensor, x: torch.Tensor, cand_ids: torch.Tensor, cand_q: torch.Tensor,
+                 r: torch.Tensor, u: torch.Tensor, stream=None):
+    """The exactness rule over B chains: p B x (Kd+1) x n, x B x Kd, cand_ids /
+    cand_q B x Kd x K, r B x Kd, u B x (Kd+1). Returns (tokens B x (Kd+1),
+    accepted counts B)."""
+    B, Kd1, n = p.shape
+    Kd = Kd1 - 1
+    K = cand_ids.shape[-1]
+    dev = p.device
+    tokens = torch.empty((B, Kd + 1), dtype=torch.int32, device=dev)
+    count = torch.empty(B, dtype=torch.int32, device=dev)
+    check(load().lmhead_verify_chain(
+        _typed(p, torch.float32, "p"), n, B, Kd, _typed(x, torch.int32, "x"),
+        _typed(cand_ids, torch.int32, "cand_ids"), _typed(cand_q, torch.float32, "cand_q"), K,
+        _typed(r, torch.float32, "r"), _typed(u, torch.float32, "u"), tokens.data_ptr(),
+        count.data_ptr(), _stream_ptr(stream)), "verify_chain")
+    return tokens, count

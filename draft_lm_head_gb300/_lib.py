@@ -32,6 +32,8 @@ SIGNATURES = {
     "lmhead_dense_head": (_I, [_P, _P, _I64, _I, _I, _F, _P, _P, _P]),
     "lmhead_pruned_head": (_I, [_P, _P, _I, _I, _I, _F, _P, _P, _P]),
     "lmhead_last_device_error": (_I, [_P]),
+    "lmhead_draft_select": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "lmhead_verify_chain": (_I, [_P, _I64, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
     "lmhead_two_stage_local_noalloc": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _F,
                                             _P, _P, _P, _P]),
 }

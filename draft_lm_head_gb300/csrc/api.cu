@@ -335,6 +335,32 @@ int lmhead_pruned_head(const lmhead_bf16* W_pruned, const lmhead_bf16* h, int n_
   return lmhead_dense_head(W_pruned, h, n_keep, d, M, temperature, out_logits, out_q, stream);
 }
 
+int lmhead_draft_select(const float* q, const int32_t* ids, int M, int K, int k_sel,
+                        const float* parent_value, const float* uniforms, int32_t* out_top_ids,
+                        float* out_top_q, float* out_top_value, int32_t* out_sample_id,
+                        float* out_sample_q, lmhead_stream stream) {
+  if (!q || !ids || !out_top_ids || !out_top_q) return LMHEAD_ERR_NULL;
+  if (M < 1 || M > 2147483647 || K < 1 || K > kSelectMaxK || k_sel < 1 || k_sel > K ||
+      k_sel > kDraftMaxK)
+    return LMHEAD_ERR_SHAPE;
+  return cuda_status(launch_draft_select(q, ids, M, K, k_sel, parent_value, uniforms, out_top_ids,
+                                         out_top_q, out_top_value, uniforms ? out_sample_id : nullptr,
+                                         uniforms ? out_sample_q : nullptr, (cudaStream_t)stream));
+}
+
+int lmhead_verify_chain(const float* p, int64_t n, int B, int Kd, const int32_t* x,
+                        const int32_t* cand_ids, const float* cand_q, int K, const float* r,
+                        const float* u, int32_t* out_tokens, int32_t* out_count,
+                        lmhead_stream stream) {
+  if (!p || !u || !out_tokens || !out_count) return LMHEAD_ERR_NULL;
+  if (Kd > 0 && (!x || !cand_ids || !cand_q || !r)) return LMHEAD_ERR_NULL;
+  if (n < 1 || n > INT32_MAX || B < 1 || B > 65535 || Kd < 0 || Kd > 1024 || K < 1 ||
+      K > kSelectMaxK)
+    return LMHEAD_ERR_SHAPE;
+  return cuda_status(launch_verify_chain(p, n, B, Kd, x, cand_ids, cand_q, K, r, u, out_tokens,
+                                         out_count, device_error_word(), (cudaStream_t)stream));
+}
+
 int lmhead_last_device_error(lmhead_stream stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LMHEAD_ERR_CUDA;
   int* p = device_error_word();

@@ -65,6 +65,20 @@ constexpr int kRowsTcMaxN = 256;
 cudaError_t launch_rows_dense_tc(const bf16_t* X, int64_t n, int kdim, const bf16_t* Y, int M,
                                  float* out, int64_t ldo, int* err, cudaStream_t s);
 
+// K8: per row, the k_sel (<= kDraftMaxK) largest q (ties: smaller id) with
+// value parent * q, and optionally a Gumbel-max draw from q (uniforms M x K).
+constexpr int kDraftMaxK = 16;
+cudaError_t launch_draft_select(const float* q, const int32_t* ids, int M, int K, int k_sel,
+                                const float* parent_value, const float* uniforms, int32_t* top_ids,
+                                float* top_q, float* top_value, int32_t* sample_id,
+                                float* sample_q, cudaStream_t s);
+// K9: chain verification of B chains of Kd drafted tokens against dense
+// target rows p (B x (Kd + 1) x n), candidate lists B x Kd x K.
+cudaError_t launch_verify_chain(const float* p, int64_t n, int B, int Kd, const int32_t* x,
+                                const int32_t* cand_ids, const float* cand_q, int K, const float* r,
+                                const float* u, int32_t* out_tokens, int32_t* out_count, int* err,
+                                cudaStream_t s);
+
 int* device_error_word();  // this device's error word (nullptr on failure)
 
 // TMA map of a rows x cols bf16 row-major matrix: box_rows x box_cols

@@ -225,6 +225,53 @@ int lmhead_two_stage_local_noalloc(const lmhead_bf16* W, const lmhead_bf16* A,
                                    float* out_logits, float* out_q, lmhead_stream stream);
 
 /*
+ * Draft-token selection on q ("EAGLE -> EAGLE-2 -> EAGLE-3 -> DFlash", the
+ * EAGLE-2 dynamic draft tree, Expansion Phase: a node is expanded into its
+ * most likely draft tokens, and a token's value is the product of the draft
+ * confidences along its path). Per row m of q (one tree node):
+ *   q, ids        M x K fp32 / int32: the node's draft distribution over its
+ *                 candidates (lmhead_two_stage's out_q and out_ids).
+ *   k_sel         1 <= k_sel <= min(K, 16).
+ *   parent_value  M fp32, the node's own value, or NULL (value 1).
+ *   uniforms      M x K fp32 in (0, 1), or NULL for no draw.
+ *   out_top_ids, out_top_q, out_top_value  M x k_sel: the k_sel largest q
+ *                 (ties: smaller vocabulary id), descending, and
+ *                 parent_value * q (fp32). out_top_value may be NULL.
+ *   out_sample_id, out_sample_q  M (may be NULL): one token drawn from q by
+ *                 Gumbel-max, argmax_j log q_j - log(-log uniforms_j) (ties:
+ *                 smaller id), and its q. Ignored when uniforms is NULL.
+ * Returns LMHEAD_ERR_SHAPE for bad sizes; everything else as above.
+ */
+int lmhead_draft_select(const float* q, const int32_t* ids, int M, int K, int k_sel,
+                        const float* parent_value, const float* uniforms, int32_t* out_top_ids,
+                        float* out_top_q, float* out_top_value, int32_t* out_sample_id,
+                        float* out_sample_q, lmhead_stream stream);
+
+/*
+ * Chain verification of drafted tokens ("Speculative decoding and EAGLE",
+ * the exactness rule): for t = 0..Kd-1, accept x_t if r_t < p_t(x_t) /
+ * q_t(x_t) (fp32); otherwise draw the replacement from (p_t - q_t)+
+ * normalised and stop; when every draft is accepted, draw a bonus token from
+ * p_Kd. q_t is the head's distribution over row t's candidates, zero
+ * elsewhere (the pointwise residual, as the page's exactness claim requires).
+ * Draws: the smallest vocabulary id v whose running sum of weights exceeds
+ * u * (total weight), in vocabulary order.
+ *   p         B x (Kd + 1) x n fp32: target distributions (rows sum to 1).
+ *   x         B x Kd int32: drafted tokens; each must be a candidate of its row.
+ *   cand_ids, cand_q  B x Kd x K: the drafter's candidates and q (1 <= K <= 4096).
+ *   r         B x Kd fp32 accept uniforms; u  B x (Kd + 1) fp32 draw uniforms.
+ *   out_tokens  B x (Kd + 1) int32: the accepted drafts, then the replacement
+ *             or bonus token, then -1; out_count  B int32: drafts accepted
+ *             (0..Kd), or -1 when a drafted token is not a candidate (also
+ *             recorded as LMHEAD_ERR_DEVICE_CHECK, see lmhead_last_device_error).
+ * One CTA per chain; Kd may be 0 (bonus draw only).
+ */
+int lmhead_verify_chain(const float* p, int64_t n, int B, int Kd, const int32_t* x,
+                        const int32_t* cand_ids, const float* cand_q, int K, const float* r,
+                        const float* u, int32_t* out_tokens, int32_t* out_count,
+                        lmhead_stream stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * word. Returns LMHEAD_OK, LMHEAD_ERR_DEVICE_CHECK, LMHEAD_ERR_TIMEOUT, or
  * LMHEAD_ERR_CUDA if the synchronisation itself failed.

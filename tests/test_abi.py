@@ -104,3 +104,21 @@ def test_validation_before_launch(lib):
     assert lib.lmhead_candidate_softmax(_p(ok), 1, 4, -1.0, _p(ok), None) == -2
     assert lib.lmhead_dense_head(_p(ok), _p(ok), 0, 64, 1, 1.0, _p(ok), None, None) == -2
     assert lib.lmhead_project_u(_p(ok), _p(ok + 4), 64, 16, 1, _p(ok), None) == -3
+
+
+def test_speculative_entry_points_validate_before_launch(lib):
+    ok = 1 << 20  # never dereferenced: validation returns first
+    P = _p(ok)
+    # draft selection: k_sel must be in [1, min(K, 16)]
+    assert lib.lmhead_draft_select(None, P, 1, 8, 2, None, None, P, P, None, None, None, None) == -1
+    assert lib.lmhead_draft_select(P, P, 1, 8, 0, None, None, P, P, None, None, None, None) == -2
+    assert lib.lmhead_draft_select(P, P, 1, 8, 9, None, None, P, P, None, None, None, None) == -2
+    assert lib.lmhead_draft_select(P, P, 1, 64, 17, None, None, P, P, None, None, None, None) == -2
+    assert lib.lmhead_draft_select(P, P, 0, 8, 2, None, None, P, P, None, None, None, None) == -2
+    assert lib.lmhead_draft_select(P, P, 1, 5000, 2, None, None, P, P, None, None, None, None) == -2
+    # chain verification
+    assert lib.lmhead_verify_chain(None, 100, 1, 2, P, P, P, 8, P, P, P, P, None) == -1
+    assert lib.lmhead_verify_chain(P, 100, 1, 2, None, P, P, 8, P, P, P, P, None) == -1
+    assert lib.lmhead_verify_chain(P, 0, 1, 2, P, P, P, 8, P, P, P, P, None) == -2
+    assert lib.lmhead_verify_chain(P, 100, 1, -1, P, P, P, 8, P, P, P, P, None) == -2
+    assert lib.lmhead_verify_chain(P, 100, 1, 2, P, P, P, 5000, P, P, P, P, None) == -2
