@@ -217,6 +217,52 @@ def aggregate_rate(world, rows_per_rank, steps, ms):
     return world * rows_per_rank * steps / (ms / 1e3)
 
 
+def time_after_q(torch, L, out, hbm, reps=50):
+    """Graph-replayed timings of the steps that consume q: EAGLE-2 draft
+    selection (top-8 per row with path values and a Gumbel-max draw) on the
+    headline call's q, and chain verification of 8 chains of 4 drafts against
+    synthetic dense target rows of the full vocabulary (seeded; the residual is
+    drawn wherever a draft is rejected)."""
+    ids, _, q = out
+    M, K = q.shape
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234)
+    U = torch.rand((M, K), generator=g, device="cuda").clamp_(1e-7, 1 - 1e-7)
+    parent = torch.rand(M, generator=g, device="cuda")
+    res = {}
+
+    def timed(fn):
+        gr = make_graph(torch, fn)
+        gr.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            gr.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / reps
+
+    us = timed(lambda: L.draft_select(q, ids, 8, parent, U))
+    by = M * K * 12 + M * 4
+    res["draft_select"] = {"M": M, "K": K, "k_sel": 8, "us": round(us, 2), "bytes": by,
+                           "hbm_frac": round(by / (us * 1e-6) / 1e9 / hbm, 4)}
+    n, Bc, Kd, Kc = WORKLOAD.n, 8, 4, K
+    p = torch.softmax(torch.randn((Bc, Kd + 1, n), generator=g, device="cuda") * 2.5, dim=-1)
+    cid = ids[:Bc * Kd].reshape(Bc, Kd, Kc).contiguous()
+    cq = q[:Bc * Kd].reshape(Bc, Kd, Kc).contiguous()
+    x = cid[:, :, 0].contiguous()            # each row's first candidate as the draft
+    r = torch.rand((Bc, Kd), generator=g, device="cuda")
+    u = torch.rand((Bc, Kd + 1), generator=g, device="cuda")
+    tok, cnt = L.verify_chain(p, x, cid, cq, r, u)
+    acc = int(cnt.sum().item())
+    us = timed(lambda: L.verify_chain(p, x, cid, cq, r, u))
+    res["verify_chain"] = {"chains": Bc, "drafts": Kd, "n": n, "K": Kc, "us": round(us, 2),
+                           "accepted_total": acc,
+                           "note": "one full-vocabulary pass of p per chain at its stop position"}
+    return res
+
+
 def run_ours(args):
     import ctypes
     global NROT
@@ -406,6 +452,10 @@ def run_ours(args):
                           "hbm_frac": round(by / (us * 1e-6) / 1e9 / hbm, 4),
                           "dense_us": round(dus, 2)})
             del g, gd
+    # the steps after q (draft selection, chain verification), for context
+    after_q = {}
+    if not args.no_sweep and rank == 0:
+        after_q = time_after_q(torch, L, outs[0], hbm)
     clocks = sampler.stop()
 
     cpu = None
@@ -431,7 +481,7 @@ def run_ours(args):
             "clocks": clocks, "kernel_us": {k: round(v, 3) for k, v in kern_us.items()},
             "step_bytes": step_bytes,
             "step_hbm_frac": round(step_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm, 4),
-            "unique_rows": U, "sweep": sweep,
+            "unique_rows": U, "sweep": sweep, "after_q": after_q,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -13,8 +13,9 @@
 // stop; when every draft is accepted, draw a bonus token from p_Kd. Draws
 // use the inverse CDF in vocabulary order with one caller-supplied uniform.
 // One CTA per chain: the candidates of the rejected position go into a
-// shared-memory hash table, each thread sums the residual over a contiguous
-// slice of the vocabulary, a block scan places the draw.
+// shared-memory hash table, warps sum the residual over contiguous runs of
+// the vocabulary with coalesced loads, and a scan of the run sums places the
+// draw.
 #include <math.h>
 
 #include "common.cuh"
@@ -123,20 +124,25 @@ __device__ __forceinline__ uint32_t hash_slot(int32_t id) {
 
 // Inverse-CDF draw over w_v = max(0, p_v - q(v)) (q from the hash table, or
 // none when use_q is false): the smallest v whose running sum exceeds u * W.
-// Each thread sums a contiguous slice of the vocabulary; one thread turns the
-// slice sums into prefix sums sequentially, so the slices' intervals
-// [start_i, start_{i+1}) partition [0, W) exactly. The thread whose interval
-// holds u * W walks its slice; if rounding keeps the walk from crossing, or
-// u * W rounds up to W, the last positive weight of the slice (of the whole
-// vocabulary) is taken. W == 0 falls back to p itself. Returns the token on
-// every thread.
+// The vocabulary is read in chunks of 32 consecutive entries (one coalesced
+// load per warp); warp w owns a contiguous run of chunks and sums it (lane
+// partials, then one warp reduction). Warp offsets chain the warp totals in
+// warp order, so every warp's interval [off_w, off_{w+1}) holds exactly the
+// targets it owns. The owning warp walks its run again in blocks of 32
+// chunks (one chunk sum per lane, a scan over them) and, in the crossing
+// chunk, takes the first entry whose running sum passes the target. Where rounding keeps a walk from crossing, or u * W rounds up
+// to W, the last positive weight of the run (of the vocabulary) is taken.
+// W == 0 falls back to p itself. Returns the token on every thread.
 __device__ int residual_draw(const float* __restrict__ prow, int64_t n, bool use_q,
-                             const int32_t* tkey, const float* tval, float u, float* start,
+                             const int32_t* tkey, const float* tval, float u, float* wtot,
                              int* s_tok) {
-  const int64_t per = (n + kVerThreads - 1) / kVerThreads;
-  const int64_t v0 = (int64_t)threadIdx.x * per;
-  const int64_t v1 = v0 + per < n ? v0 + per : n;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kWarps = kVerThreads / 32;
+  const int64_t nch = (n + 31) / 32;
+  const int64_t cpw = (nch + kWarps - 1) / kWarps;
+  const int64_t c0 = warp * cpw, c1 = c0 + cpw < nch ? c0 + cpw : nch;
   auto weight = [&](int64_t v, bool sub) -> float {
+    if (v >= n) return 0.f;
     float w = prow[v];
     if (sub) {
       uint32_t h = hash_slot((int32_t)v);
@@ -151,44 +157,77 @@ __device__ int residual_draw(const float* __restrict__ prow, int64_t n, bool use
   };
   for (int pass = 0; pass < 2; ++pass) {
     const bool sub = use_q && pass == 0;
-    float local = 0.f;
-    for (int64_t v = v0; v < v1; ++v) local += weight(v, sub);
-    start[threadIdx.x + 1] = local;
+    float part = 0.f;  // this lane's share of the run (coalesced loads, no shuffles)
+#pragma unroll 8
+    for (int64_t c = c0; c < c1; ++c) part += weight(c * 32 + lane, sub);
+    const float run = warp_sum(part);  // identical in every lane
+    if (lane == 0) wtot[warp] = run;
+    if (threadIdx.x == 0) *s_tok = -1;
     cta_sync();
-    if (threadIdx.x == 0) {
-      float acc = 0.f;
-      start[0] = 0.f;
-      for (int i = 1; i <= kVerThreads; ++i) {
-        acc += start[i];
-        start[i] = acc;
-      }
-      *s_tok = -1;
+    float off = 0.f, total = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w == warp) off = total;
+      total += wtot[w];
     }
-    cta_sync();
-    const float total = start[kVerThreads];
+    const float hi = warp + 1 < kWarps ? off + wtot[warp] : total;
     if (!(total > 0.f)) {  // (p - q)+ vanishes: draw from p
       cta_sync();
       continue;
     }
     const float target = u * total;
-    const float lo = start[threadIdx.x], hi = start[threadIdx.x + 1];
-    if (lo <= target && target < hi) {
-      float acc = lo;
+    if (off <= target && target < hi) {
+      // walk the run in blocks of 32 chunks: lane L sums chunk b + L (its
+      // loads are independent), a scan over the 32 chunk sums and a ballot
+      // find the crossing chunk, a scan over its 32 lanes the entry
+      float acc = off;
       int64_t pick = -1, last_pos = -1;
-      for (int64_t v = v0; v < v1; ++v) {
-        const float w = weight(v, sub);
-        if (w > 0.f) last_pos = v;
-        acc += w;
-        if (acc > target) { pick = v; break; }
+      for (int64_t b = c0; b < c1 && pick < 0; b += 32) {
+        const int64_t c = b + lane;
+        float cs = 0.f;
+        if (c < c1) {
+#pragma unroll 8
+          for (int i = 0; i < 32; ++i) cs += weight(c * 32 + i, sub);
+        }
+        float sc = cs;  // inclusive scan of the chunk sums
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float t = __shfl_up_sync(0xFFFFFFFFu, sc, o);
+          if (lane >= o) sc += t;
+        }
+        const uint32_t pos = __ballot_sync(0xFFFFFFFFu, cs > 0.f);
+        if (pos) last_pos = b + 31 - __clz(pos);  // last chunk with weight (refined below)
+        const uint32_t cross = __ballot_sync(0xFFFFFFFFu, c < c1 && cs > 0.f && acc + sc > target);
+        if (cross) {
+          const int k = __ffs(cross) - 1;
+          const float before = acc + __shfl_sync(0xFFFFFFFFu, sc - cs, k);
+          const int64_t cc = b + k;
+          const float wl = weight(cc * 32 + lane, sub);
+          float se = wl;  // inclusive scan over the chunk's entries
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_up_sync(0xFFFFFFFFu, se, o);
+            if (lane >= o) se += t;
+          }
+          const uint32_t hit = __ballot_sync(0xFFFFFFFFu, wl > 0.f && before + se > target);
+          const uint32_t wpos = __ballot_sync(0xFFFFFFFFu, wl > 0.f);
+          pick = hit ? cc * 32 + __ffs(hit) - 1 : cc * 32 + 31 - __clz(wpos);
+        }
+        acc += __shfl_sync(0xFFFFFFFFu, sc, 31);
       }
-      *s_tok = (int)(pick >= 0 ? pick : last_pos);
+      if (pick < 0 && last_pos >= 0) {  // rounding kept the walk short: last positive entry
+        const uint32_t wpos = __ballot_sync(0xFFFFFFFFu, weight(last_pos * 32 + lane, sub) > 0.f);
+        pick = last_pos * 32 + 31 - __clz(wpos);
+      }
+      if (lane == 0) *s_tok = (int)pick;
     }
     cta_sync();
-    if (*s_tok < 0 && hi > lo) {  // target at or past W: the last positive weight
+    if (*s_tok < 0 && wtot[warp] > 0.f) {  // target at or past W: the last positive weight
       int64_t last_pos = -1;
-      for (int64_t v = v1 - 1; v >= v0; --v)
-        if (weight(v, sub) > 0.f) { last_pos = v; break; }
-      if (last_pos >= 0) atomicMax(s_tok, (int)last_pos);
+      for (int64_t c = c1 - 1; c >= c0 && last_pos < 0; --c) {
+        const uint32_t pos = __ballot_sync(0xFFFFFFFFu, weight(c * 32 + lane, sub) > 0.f);
+        if (pos) last_pos = c * 32 + 31 - __clz(pos);
+      }
+      if (lane == 0 && last_pos >= 0) atomicMax(s_tok, (int)last_pos);
     }
     cta_sync();
     const int tok = *s_tok;
@@ -207,7 +246,7 @@ verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_
   extern __shared__ int32_t vsm[];
   int32_t* tkey = vsm;                                          // [kHashSlots]
   float* tval = reinterpret_cast<float*>(vsm + kHashSlots);     // [kHashSlots]
-  __shared__ float start[kVerThreads + 1];
+  __shared__ float wtot[kVerThreads / 32];
   __shared__ int s_hit, s_tok;
   const int b = blockIdx.x;
   const float* pb = p + (size_t)b * (Kd + 1) * n;
@@ -255,7 +294,7 @@ verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_
     }
     cta_sync();
     const int tok = residual_draw(pb + (size_t)t * n, n, true, tkey, tval,
-                                  u[(size_t)b * (Kd + 1) + t], start, &s_tok);
+                                  u[(size_t)b * (Kd + 1) + t], wtot, &s_tok);
     if (threadIdx.x == 0) {
       ob[t] = tok;
       out_count[b] = t;
@@ -263,7 +302,7 @@ verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_
     return;
   }
   const int tok = residual_draw(pb + (size_t)Kd * n, n, false, tkey, tval,
-                                u[(size_t)b * (Kd + 1) + Kd], start, &s_tok);
+                                u[(size_t)b * (Kd + 1) + Kd], wtot, &s_tok);
   if (threadIdx.x == 0) {
     ob[Kd] = tok;
     out_count[b] = Kd;
