@@ -130,8 +130,9 @@ __device__ __forceinline__ uint32_t hash_slot(int32_t id) {
 // warp order, so every warp's interval [off_w, off_{w+1}) holds exactly the
 // targets it owns. The owning warp walks its run again in blocks of 32
 // chunks (one chunk sum per lane, a scan over them) and, in the crossing
-// chunk, takes the first entry whose running sum passes the target. Where rounding keeps a walk from crossing, or u * W rounds up
-// to W, the last positive weight of the run (of the vocabulary) is taken.
+// chunk, takes the first entry whose running sum passes the target. Where
+// rounding keeps a walk from crossing, or u * W rounds up to W, the last
+// positive weight of the run (of the vocabulary) is taken.
 // W == 0 falls back to p itself. Returns the token on every thread.
 __device__ int residual_draw(const float* __restrict__ prow, int64_t n, bool use_q,
                              const int32_t* tkey, const float* tval, float u, float* wtot,
