@@ -151,3 +151,55 @@ def test_workload4_dense_and_pruned(L, M):
     P.check_logits(host(lp)[rows], Z[:, keep])
     for i, m in enumerate(rows):
         assert np.abs(host(qp)[m] - O.candidate_softmax(Z[i, keep])).max() < P.Q_ABS
+
+
+def test_workload2_draft_select_and_verify(L):
+    # the steps after q on the headline head: q and ids from the two-stage call,
+    # targets p = the dense head's full-vocabulary softmax of the same hidden vectors
+    import torch
+    wl = synth.workload(2)
+    Bc, Kd = 4, 3
+    M = Bc * (Kd + 1)
+    case = workload_case(wl, M)
+    W, A, B = dev_bf16(case["W"]), dev_bf16(case["A"]), dev_bf16(case["B"])
+    h, tok = dev_bf16(case["h"]), dev_i32(case["tok"])
+    ids, lg, q = L.two_stage(L.LOCAL, W, A, B, h, tok, wl.T, wl.k_tile, temperature=0.8)
+    _, p = L.dense_head(W, h, 0.8)
+    rng = np.random.default_rng(7)
+    K = ids.shape[1]
+    U = np.clip(rng.random((M, K)), 1e-7, 1 - 1e-7).astype(np.float32)
+    parent = rng.random(M).astype(np.float32)
+    ti, tq, tv, si, sq = L.draft_select(q, ids, 8, torch.from_numpy(parent).cuda(),
+                                        torch.from_numpy(U).cuda())
+    qh, ih = host(q), host(ids)
+    for m in range(M):
+        oi, oq, ov = O.draft_topk(qh[m], ih[m], 8, parent[m])
+        assert np.array_equal(host(ti)[m], oi) and np.array_equal(host(tv)[m], ov)
+        gid, gj, s = O.gumbel_sample(qh[m], ih[m], U[m].astype(np.float64))
+        j = int(np.nonzero(ih[m] == host(si)[m])[0][0])
+        assert s[gj] - s[j] <= 1e-5 * (1 + abs(s[gj]))
+    # chains: row (b, t) of the batch is position t of chain b; drafts are the draws above
+    rows = np.arange(M).reshape(Bc, Kd + 1)
+    ph = host(p).reshape(Bc, Kd + 1, -1)
+    cid = ih[rows[:, :Kd]]
+    cq = qh[rows[:, :Kd]]
+    x = host(si)[rows[:, :Kd]].astype(np.int32)
+    r = rng.random((Bc, Kd)).astype(np.float32)
+    u = rng.random((Bc, Kd + 1)).astype(np.float32)
+    tokens, count = L.verify_chain(p.reshape(Bc, Kd + 1, -1).contiguous(),
+                                   torch.from_numpy(x).cuda(), torch.from_numpy(cid).cuda(),
+                                   torch.from_numpy(cq).cuda(), torch.from_numpy(r).cuda(),
+                                   torch.from_numpy(u).cuda())
+    tokens, count = host(tokens), host(count)
+    for b in range(Bc):
+        n_acc, out = O.verify_chain(ph[b], x[b], cid[b], cq[b], r[b], u[b])
+        assert count[b] == n_acc and list(tokens[b, :n_acc]) == out[:n_acc]
+        vg, vo = int(tokens[b, n_acc]), out[n_acc]
+        if vg != vo:
+            w = ph[b, n_acc].astype(np.float64) if n_acc == Kd else \
+                O.residual(ph[b, n_acc], cid[b, n_acc], cq[b, n_acc])
+            c = np.cumsum(w)
+            target = float(u[b, n_acc]) * c[-1]
+            lo = c[vg - 1] if vg > 0 else 0.0
+            assert w[vg] > 0 and lo - 1e-4 * c[-1] <= target <= c[vg] + 1e-4 * c[-1]
+    assert L.last_device_error() == 0
