@@ -263,6 +263,54 @@ def time_after_q(torch, L, out, hbm, reps=50):
     return res
 
 
+def time_cluster(torch, L, head, rot_h, hbm, group=128, G=8, reps=40):
+    """Graph-replayed timings of the cluster-level route on the same head (A
+    in vocabulary order, groups of `group` consecutive rows, the G best groups
+    per hidden vector, G*group = 1024 candidates like the global route's C)
+    at M = 1 and 64, with the algorithmic bytes: A, B, h once, each distinct
+    selected group's W block once, outputs."""
+    n, d = head["W"].shape
+    r = head["B"].shape[0]
+    A_voc = np.empty_like(head["A"])
+    A_voc[head["tok"]] = head["A"]
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    copies = [(rt[0], dev(A_voc), rt[2]) for rt in rot_h]  # the headline's W and B copies
+    ws = L.Workspace()
+    res = []
+    for Mx in (1, 64):
+        hs = [dev(hidden(head["W"], Mx, 0)) for _ in copies]
+        K = G * group
+        outs = [(torch.empty((Mx, G), dtype=torch.int32, device="cuda"),
+                 torch.empty((Mx, K), dtype=torch.int32, device="cuda"),
+                 torch.empty((Mx, K), dtype=torch.float32, device="cuda"),
+                 torch.empty((Mx, K), dtype=torch.float32, device="cuda")) for _ in copies]
+
+        def calls():
+            for j, (Wt, At, Bt) in enumerate(copies):
+                L.cluster_two_stage(Wt, At, Bt, hs[j], group, G, workspace=ws, out=outs[j])
+
+        gr = make_graph(torch, calls)
+        gr.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps // len(copies)):
+            gr.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps // len(copies) * len(copies))
+        Ug = int(np.unique(outs[0][0].cpu().numpy()).size)
+        by = 2 * n * r + 2 * r * d + 2 * Mx * d + 2 * d * group * Ug + Mx * (4 * G + 12 * K)
+        res.append({"M": Mx, "group": group, "G": G, "candidates": K, "us": round(us, 2),
+                    "vecs_per_s": round(Mx / us * 1e6, 1), "unique_groups": Ug, "bytes": by,
+                    "hbm_frac": round(by / (us * 1e-6) / 1e9 / hbm, 4)})
+        del gr
+    return res
+
+
 def run_ours(args):
     import ctypes
     global NROT
@@ -480,8 +528,10 @@ def run_ours(args):
             del g, gd
     # the steps after q (draft selection, chain verification), for context
     after_q = {}
+    cluster = []
     if not args.no_sweep and rank == 0:
         after_q = time_after_q(torch, L, outs[0], hbm)
+        cluster = time_cluster(torch, L, head, rot, hbm)
     clocks = sampler.stop()
 
     cpu = None
@@ -507,7 +557,7 @@ def run_ours(args):
             "clocks": clocks, "kernel_us": {k: round(v, 3) for k, v in kern_us.items()},
             "step_bytes": step_bytes,
             "step_hbm_frac": round(step_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm, 4),
-            "unique_rows": U, "sweep": sweep, "after_q": after_q,
+            "unique_rows": U, "sweep": sweep, "after_q": after_q, "cluster_route": cluster,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

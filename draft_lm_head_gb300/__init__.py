@@ -26,7 +26,8 @@ LOCAL = 1
 __all__ = [
     "GLOBAL", "LOCAL", "LmheadError", "candidate_count", "workspace_size", "project_u",
     "lowrank_score_topk", "gather_logits", "candidate_softmax", "two_stage", "dense_head",
-    "pruned_head", "draft_select", "verify_chain", "last_device_error", "version", "Workspace",
+    "pruned_head", "cluster_candidate_count", "cluster_workspace_size", "cluster_two_stage",
+    "draft_select", "verify_chain", "last_device_error", "version", "Workspace",
 ]
 
 _BF16_OK = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (
@@ -200,6 +201,48 @@ def pruned_head(W_pruned: torch.Tensor, h: torch.Tensor, temperature: float = 1.
 def last_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return int(load().lmhead_last_device_error(_stream_ptr(stream)))
+
+
+@functools.lru_cache(maxsize=4096)
+def cluster_candidate_count(n: int, group: int, G: int) -> int:
+    K = load().lmhead_cluster_candidate_count(n, group, G)
+    if K < 0:
+        raise LmheadError(int(K), "cluster_candidate_count")
+    return int(K)
+
+
+@functools.lru_cache(maxsize=4096)
+def cluster_workspace_size(n: int, d: int, r: int, M: int, group: int, G: int) -> int:
+    return int(load().lmhead_cluster_workspace_size(n, d, r, M, group, G))
+
+
+def cluster_two_stage(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, h: torch.Tensor,
+                      group: int, G: int, temperature: float = 1.0, with_group_scores=False,
+                      workspace=None, out=None, stream=None):
+    """The cluster-level head: returns (groups M x G, ids, logits, q each
+    M x G*group), plus the groups' scores when with_group_scores."""
+    n, d = W.shape
+    r = A.shape[1]
+    M = h.shape[0]
+    K = cluster_candidate_count(n, group, G)
+    dev = h.device
+    if out is None:
+        groups = torch.empty((M, G), dtype=torch.int32, device=dev)
+        ids = torch.empty((M, K), dtype=torch.int32, device=dev)
+        L = torch.empty((M, K), dtype=torch.float32, device=dev)
+        q = torch.empty((M, K), dtype=torch.float32, device=dev)
+    else:
+        groups, ids, L, q = out
+    gs = torch.empty((M, G), dtype=torch.float32, device=dev) if with_group_scores else None
+    nbytes = cluster_workspace_size(n, d, r, M, group, G)
+    ws = _ws(workspace, nbytes, dev)
+    check(load().lmhead_cluster_two_stage(
+        _bf16(W, "W"), _bf16(A, "A"), _bf16(B, "B"), _bf16(h, "h"), n, d, r, M, group, G,
+        float(temperature), _typed(groups, torch.int32, "groups"),
+        _typed(gs, torch.float32, "group_scores"), _typed(ids, torch.int32, "ids"),
+        _typed(L, torch.float32, "logits"), _typed(q, torch.float32, "q"), ws.data_ptr(),
+        ws.numel(), _stream_ptr(stream)), "cluster_two_stage")
+    return (groups, ids, L, q, gs) if with_group_scores else (groups, ids, L, q)
 
 
 def draft_select(q: torch.Tensor, ids: torch.Tensor, k_sel: int,

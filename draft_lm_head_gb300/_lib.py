@@ -34,6 +34,10 @@ SIGNATURES = {
     "lmhead_last_device_error": (_I, [_P]),
     "lmhead_draft_select": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "lmhead_verify_chain": (_I, [_P, _I64, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
+    "lmhead_cluster_candidate_count": (_I64, [_I64, _I, _I]),
+    "lmhead_cluster_workspace_size": (_SZ, [_I64, _I, _I, _I, _I, _I]),
+    "lmhead_cluster_two_stage": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _F,
+                                      _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "lmhead_two_stage_local_noalloc": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _F,
                                             _P, _P, _P, _P]),
 }

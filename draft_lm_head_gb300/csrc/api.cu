@@ -165,6 +165,40 @@ int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
   return LMHEAD_OK;
 }
 
+// Cluster-level route: the local selection with one candidate per group
+// (tile = group, k_tile = 1) leaves every group's best score in the
+// workspace; the segment top-k picks the G best groups from those.
+struct ClusterLayout {
+  Layout sel;
+  size_t best_ids = 0, gscores = 0, total = 0;
+};
+
+int64_t cluster_count(int64_t n, int group, int G) {
+  if (n < 1 || n > INT32_MAX || group < 1 || n % group) return LMHEAD_ERR_SHAPE;
+  if (G < 1 || G > n / group) return LMHEAD_ERR_SHAPE;
+  return (int64_t)G * group;
+}
+
+int check_cluster(int64_t n, int d, int r, int M, int group, int G) {
+  const int64_t K = cluster_count(n, group, G);
+  if (K < 0) return (int)K;
+  const int st = check_select(LMHEAD_LOCAL, n, d, r, M, group, 1);
+  if (st != LMHEAD_OK) return st;
+  if (G > kSelectMaxK) return LMHEAD_ERR_UNSUPPORTED;
+  if ((int64_t)M * K > INT32_MAX || (int64_t)M * (n / group) > INT32_MAX) return LMHEAD_ERR_SHAPE;
+  return LMHEAD_OK;
+}
+
+ClusterLayout cluster_layout(int64_t n, int d, int r, int M, int group) {
+  ClusterLayout C;
+  C.sel = layout_for(LMHEAD_LOCAL, n, d, r, M, group, 1);
+  const size_t cells = (size_t)M * (size_t)(n / group);
+  C.best_ids = round_up(C.sel.total, 256);
+  C.gscores = round_up(C.best_ids + cells * sizeof(int32_t), 256);
+  C.total = round_up(C.gscores + cells * sizeof(float), 256);
+  return C;
+}
+
 int launches_for(int mode, int k_tile) { return needs_score_buffer(mode, k_tile) ? 5 : 4; }
 
 bool valid_temperature(float t) { return t > 0.f && isfinite(t); }
@@ -359,6 +393,53 @@ int lmhead_verify_chain(const float* p, int64_t n, int B, int Kd, const int32_t*
     return LMHEAD_ERR_SHAPE;
   return cuda_status(launch_verify_chain(p, n, B, Kd, x, cand_ids, cand_q, K, r, u, out_tokens,
                                          out_count, device_error_word(), (cudaStream_t)stream));
+}
+
+int64_t lmhead_cluster_candidate_count(int64_t n, int group, int G) {
+  return cluster_count(n, group, G);
+}
+
+size_t lmhead_cluster_workspace_size(int64_t n, int d, int r, int M, int group, int G) {
+  if (check_cluster(n, d, r, M, group, G) != LMHEAD_OK) return 0;
+  return cluster_layout(n, d, r, M, group).total;
+}
+
+int lmhead_cluster_two_stage(const lmhead_bf16* W, const lmhead_bf16* A, const lmhead_bf16* B,
+                             const lmhead_bf16* h, int64_t n, int d, int r, int M, int group,
+                             int G, float temperature, int32_t* out_groups,
+                             float* out_group_scores, int32_t* out_ids, float* out_logits,
+                             float* out_q, void* workspace, size_t workspace_bytes,
+                             lmhead_stream stream) {
+  if (!W || !A || !B || !h || !out_groups || !out_ids || !out_logits || !out_q)
+    return LMHEAD_ERR_NULL;
+  int st = check_cluster(n, d, r, M, group, G);
+  if (st != LMHEAD_OK) return st;
+  if (!valid_temperature(temperature)) return LMHEAD_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(A) || !aligned16(B) || !aligned16(h)) return LMHEAD_ERR_ALIGN;
+  const ClusterLayout C = cluster_layout(n, d, r, M, group);
+  if (!workspace || workspace_bytes < C.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return LMHEAD_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* best_ids = reinterpret_cast<int32_t*>(ws + C.best_ids);
+  float* gscores = reinterpret_cast<float*>(ws + C.gscores);
+  Marks none;
+  // stage 1: every group's best low-rank score, then the G best groups
+  st = run_select(LMHEAD_LOCAL, A, B, h, nullptr, n, d, r, M, group, 1, best_ids, gscores, ws,
+                  C.sel, true, none, s);
+  if (st != LMHEAD_OK) return st;
+  const int64_t ngroups = n / group;
+  const int K = G * group;
+  cudaError_t e = launch_segment_topk(gscores, nullptr, ngroups, M, ngroups, G, out_groups,
+                                      out_group_scores, device_error_word(), s);
+  if (e == cudaSuccess)
+    e = launch_expand_groups(out_groups, M, G, group, ngroups, out_ids, device_error_word(), s);
+  // stage 2: exact logits of every row of the selected groups, then softmax
+  if (e == cudaSuccess)
+    e = launch_gather_logits(W, h, out_ids, n, d, M, K, out_logits, nullptr, 1.f, nullptr,
+                             device_error_word(), s, 0);
+  if (e == cudaSuccess) e = launch_row_softmax(out_logits, M, K, 1.f / temperature, out_q, s);
+  return cuda_status(e);
 }
 
 int lmhead_last_device_error(lmhead_stream stream) {

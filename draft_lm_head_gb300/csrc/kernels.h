@@ -65,6 +65,10 @@ constexpr int kRowsTcMaxN = 256;
 cudaError_t launch_rows_dense_tc(const bf16_t* X, int64_t n, int kdim, const bf16_t* Y, int M,
                                  float* out, int64_t ldo, int* err, cudaStream_t s);
 
+// Cluster-level route: ids[m, j*group + t] = groups[m, j]*group + t (M x G*group).
+cudaError_t launch_expand_groups(const int32_t* groups, int M, int G, int group, int64_t ngroups,
+                                 int32_t* ids, int* err, cudaStream_t s);
+
 // K8: per row, the k_sel (<= kDraftMaxK) largest q (ties: smaller id) with
 // value parent * q, and optionally a Gumbel-max draw from q (uniforms M x K).
 constexpr int kDraftMaxK = 16;

@@ -225,6 +225,42 @@ int lmhead_two_stage_local_noalloc(const lmhead_bf16* W, const lmhead_bf16* A,
                                    float* out_logits, float* out_q, lmhead_stream stream);
 
 /*
+ * Cluster-level two-stage head: the third route of the EAGLE-4 notes,
+ * "EAGLE Efficient LM Head" (split the tokens into groups, 128 per group in
+ * the notes' example; select a few groups; compute the logits of every token
+ * inside them and sample from those). The notes leave the group make-up and
+ * the selector open; this library reads them as:
+ *   - a group is `group` consecutive rows of the head as stored, group g =
+ *     rows [g*group, (g+1)*group), so every selected group is one contiguous
+ *     block of W; `group` must divide n;
+ *   - a group's score is the largest low-rank score A(Bh) among its rows
+ *     (the token-level route's own first stage, u rounded to bf16), and each
+ *     row of h keeps the G best groups, best first, ties by the smaller
+ *     group index.
+ * Per row m of h (M x d):
+ *   out_groups        M x G int32 selected group indices, best first.
+ *   out_group_scores  M x G fp32 their scores, or NULL.
+ *   out_ids           M x (G*group) int32: the rows of each selected group in
+ *                     selection order, ascending within a group.
+ *   out_logits, out_q M x (G*group) fp32: exact W[ids].h and their softmax
+ *                     (temperature > 0).
+ * Sizes: 1 <= G <= n/group, G <= 4096, M*G*group <= 2^31-1, d and r as for
+ * lmhead_two_stage. Scratch from `workspace`, at least
+ * lmhead_cluster_workspace_size bytes, 256-byte aligned. W, A, B, h must be
+ * 16-byte aligned (LMHEAD_ERR_ALIGN otherwise); bad sizes give
+ * LMHEAD_ERR_SHAPE (a group size that does not divide n included) and
+ * nothing is enqueued. Six kernels, no host synchronisation.
+ */
+int64_t lmhead_cluster_candidate_count(int64_t n, int group, int G);
+size_t lmhead_cluster_workspace_size(int64_t n, int d, int r, int M, int group, int G);
+int lmhead_cluster_two_stage(const lmhead_bf16* W, const lmhead_bf16* A, const lmhead_bf16* B,
+                             const lmhead_bf16* h, int64_t n, int d, int r, int M, int group,
+                             int G, float temperature, int32_t* out_groups,
+                             float* out_group_scores, int32_t* out_ids, float* out_logits,
+                             float* out_q, void* workspace, size_t workspace_bytes,
+                             lmhead_stream stream);
+
+/*
  * Draft-token selection on q ("EAGLE -> EAGLE-2 -> EAGLE-3 -> DFlash", the
  * EAGLE-2 dynamic draft tree, Expansion Phase: a node is expanded into its
  * most likely draft tokens, and a token's value is the product of the draft

@@ -133,3 +133,22 @@ def check_q(gpu_q, exact_L, temperature=1.0):
         if err > Q_ABS:
             raise AssertionError(f"q row {m}: max abs error {err:.3g}")
         assert abs(gpu_q[m].sum() - 1.0) < 1e-3
+
+
+def check_groups(gpu_groups, scores_pos, group, G, slack_pos=None):
+    """Cluster-level selection: per row, the GPU's G groups equal the
+    oracle's G best groups by their best low-rank score, except at boundary
+    ranks (same band as check_ids, the slack of a group being its rows'
+    largest). Scores are by row of the head as stored (no shuffle).
+    Returns the number of excused groups."""
+    M, n = scores_pos.shape
+    ng = n // group
+    excused = 0
+    for m in range(M):
+        gsc = O.group_scores(scores_pos[m], group)
+        gsl = (np.zeros(ng) if slack_pos is None
+               else np.asarray(slack_pos[m]).reshape(ng, group).max(axis=1))
+        ora = O.select_groups(gsc, G)
+        excused += _check_set(np.asarray(gpu_groups[m]), ora, gsc, gsl, gsc[ora[-1]], ora[-1],
+                              f"row {m} groups")
+    return excused

@@ -122,3 +122,31 @@ def test_speculative_entry_points_validate_before_launch(lib):
     assert lib.lmhead_verify_chain(P, 0, 1, 2, P, P, P, 8, P, P, P, P, None) == -2
     assert lib.lmhead_verify_chain(P, 100, 1, -1, P, P, P, 8, P, P, P, P, None) == -2
     assert lib.lmhead_verify_chain(P, 100, 1, 2, P, P, P, 5000, P, P, P, P, None) == -2
+
+
+def test_cluster_entry_points_validate_before_launch(lib):
+    ok = 1 << 20  # never dereferenced: validation returns first
+    P = _p(ok)
+    assert lib.lmhead_cluster_candidate_count(128256, 128, 8) == 1024
+    assert lib.lmhead_cluster_candidate_count(128256, 128, 1002) == 128256
+    assert lib.lmhead_cluster_candidate_count(128256, 128, 1003) == -2  # more groups than exist
+    assert lib.lmhead_cluster_candidate_count(1000, 128, 2) == -2  # ragged last group
+    assert lib.lmhead_cluster_candidate_count(1024, 0, 2) == -2
+    assert lib.lmhead_cluster_candidate_count(1024, 128, 0) == -2
+    assert lib.lmhead_cluster_workspace_size(128256, 4096, 256, 64, 128, 8) > 64 * 1002 * 8
+    assert lib.lmhead_cluster_workspace_size(1000, 4096, 256, 64, 128, 8) == 0
+
+    def call(W=P, n=4096, d=256, r=32, M=1, group=128, G=4, T=1.0, groups=P, ws=P, wsb=1 << 30):
+        return lib.lmhead_cluster_two_stage(W, P, P, P, n, d, r, M, group, G, T, groups, None, P,
+                                            P, P, ws, wsb, None)
+
+    assert call(W=None) == -1
+    assert call(groups=None) == -1
+    assert call(n=4000) == -2  # 128 does not divide n
+    assert call(G=33) == -2
+    assert call(d=100) == -2
+    assert call(T=0.0) == -2
+    assert call(n=1 << 20, group=128, G=4097) == -5  # past the group selector's budget
+    assert call(W=_p(ok + 8)) == -3
+    assert call(ws=None) == -4
+    assert call(wsb=16) == -4
