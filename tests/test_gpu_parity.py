@@ -63,6 +63,7 @@ def test_local_select(L, small, M, T, k):
     P.check_ids("local", host(ids), S, case["tok"], T, k, slack_pos=SL)
     P.check_order("local", host(ids), host(sc), T, k, case["n"])
     assert ids.shape[1] == O.local_candidate_count(case["n"], T, k)
+    assert L.last_device_error() == 0
 
 
 @pytest.mark.parametrize("M", [1, 5])
@@ -241,6 +242,21 @@ def test_two_stage_larger_m(L, M, T, k):
     P.check_logits(host(lg), ex)
     P.check_q(host(q), ex, 0.7)
     assert L.last_device_error() == 0
+
+
+# Tiles of many 128-row chunks with a long per-tile list: the scoring kernel's
+# epilogue then trails its MMAs by several chunks when the end of the work is
+# signalled (the end marker must wait for its accumulator slot like a chunk).
+@pytest.mark.parametrize("M", [1, 17, 33, 64, 150])
+@pytest.mark.parametrize("n,T,k", [(1500, 4096, 8), (5000, 1024, 8), (5000, 2048, 4)])
+def test_local_long_tiles(L, M, n, T, k):
+    case = make_case(n, 64, 16, M, seed=19, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    ids, sc = L.lowrank_score_topk(L.LOCAL, A, B, h, tok, T, k, with_scores=True)
+    assert L.last_device_error() == 0
+    _, S, _, SL = oracle_scores(case, with_slack=True)
+    P.check_ids("local", host(ids), S, case["tok"], T, k, slack_pos=SL)
+    P.check_order("local", host(ids), host(sc), T, k, n)
 
 
 @pytest.mark.parametrize("M", [1, 17, 300])
