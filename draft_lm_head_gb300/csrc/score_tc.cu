@@ -551,7 +551,7 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
   return r != 0;
 }
 
-template <int KT>
+template <int KT, int CH>
 __global__ void __launch_bounds__(kThreads, 1)
 local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
                          const __grid_constant__ CUtensorMap umap, const Params p) {
@@ -560,16 +560,19 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
   __shared__ int desc_tile[kDescRing], desc_chunk[kDescRing];
   uint8_t* dsmem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int kSt = CH * 128;                  // one CH-row x 64-element box of A
+  constexpr int kNAcc = kTmemCols / CH;          // TMEM accumulators of CH columns
+  constexpr uint32_t kIdescCH = tc::idesc_bf16_f32(kHid, CH);
   const int kblocks = (p.r + kKBlock - 1) / kKBlock;
   uint8_t* u_s = dsmem;
-  uint8_t* stage_s = dsmem + (size_t)kblocks * kStageBytes;
-  float2* xchg = reinterpret_cast<float2*>(stage_s + (size_t)p.stages * kStageBytes);  // [128][KT]
+  uint8_t* stage_s = dsmem + (size_t)kblocks * kStageBytes;  // u: 128 rows per K-block
+  float2* xchg = reinterpret_cast<float2*>(stage_s + (size_t)p.stages * kSt);  // [128][KT]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int y = blockIdx.y;
   const int NS = p.stages;
   const int64_t n = p.n, T = p.T;
-  const int cpt = (int)(T / kChunk);  // chunks per tile
+  const int cpt = (int)(T / CH);  // chunks per tile
   int* counter = p.tile_tickets + y;
   volatile int* abort_flag = &ctl.abort;
 
@@ -602,7 +605,9 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
       tc::prefetch_tmap(&umap);
       uint32_t it = 0;  // stage sequence
       int c = 0;        // chunk sequence
-      const int grp = min(min(4, NS), kblocks);
+      // 128-row boxes go in groups of four (each row's 128-byte pieces requested
+      // together); 256-row boxes, four to a small ring, one at a time
+      const int grp = CH == 256 ? 1 : min(min(4, NS), kblocks);
       bool ok = true, u_loaded = false;
       // u is written by the previous kernel: wait for it, then load it once
       auto load_u = [&]() {
@@ -635,8 +640,8 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
         }
         for (int j = 0; j < cpt && ok; ++j) {
           const int64_t gc = tile * cpt + j;  // global chunk
-          if (gc * kChunk >= n) break;
-          const bool last = j == cpt - 1 || (gc + 1) * kChunk >= n;
+          if (gc * CH >= n) break;
+          const bool last = j == cpt - 1 || (gc + 1) * CH >= n;
           desc_tile[c % kDescRing] = (int)tile;
           desc_chunk[c % kDescRing] = j | (last ? (int)0x80000000 : 0);
           // a group of up to four boxes (one chunk at r = 256) is issued back to
@@ -659,9 +664,9 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
             if (!ok) break;
             for (int g2 = 0; g2 < gcount; ++g2, ++it) {
               const int s = (int)(it % NS);
-              tc::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
-              tc::tma_load_2d(stage_s + (size_t)s * kStageBytes, &amap, &ctl.full[s],
-                              (kb0 + g2) * kKBlock, (int)(gc * kChunk));
+              tc::mbar_arrive_expect_tx(&ctl.full[s], kSt);
+              tc::tma_load_2d(stage_s + (size_t)s * kSt, &amap, &ctl.full[s],
+                              (kb0 + g2) * kKBlock, (int)(gc * CH));
             }
             // ring filled, or the first tile fully issued: u next
             if (!u_loaded && (it >= (uint32_t)NS || (j == cpt - 1 && kb0 + gcount == kblocks)))
@@ -698,28 +703,28 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
       bool ok = tc::mbar_wait(&ctl.ufull, 0, abort_flag);
       uint32_t it = 0;
       for (int c = 0; ok; ++c) {
-        const int a = c % kAcc;
+        const int a = c % kNAcc;
         int s = (int)(it % NS);
         if (!tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag)) { ok = false; break; }
         // the slot must be free before anything, the end marker included, is
         // signalled on it: an arrival two phases ahead of the epilogue's wait
         // would hide the phase it waits for
-        if (!tc::mbar_wait(&ctl.acc_empty[a], ((c / kAcc) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(&ctl.acc_empty[a], ((c / kNAcc) & 1) ^ 1, abort_flag)) { ok = false; break; }
         if (desc_tile[c % kDescRing] < 0) {  // end marker: pass it on to the epilogue
           tc::mbar_arrive(&ctl.acc_full[a]);
           break;
         }
         tc::fence_after_sync();
-        const uint32_t d = tmem + a * kChunk;
+        const uint32_t d = tmem + a * CH;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           s = (int)(it % NS);
           if (kb > 0 && !tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag)) { ok = false; break; }
           tc::fence_after_sync();
           const uint64_t adesc = tc::sw128_kmajor_desc(tc::smem_addr(u_s + (size_t)kb * kStageBytes));
-          const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_addr(stage_s + (size_t)s * kStageBytes));
+          const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_addr(stage_s + (size_t)s * kSt));
           const int nk = min(4, (p.r - kb * kKBlock + 15) / 16);
           for (int k = 0; k < nk; ++k)
-            tc::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, (kb | k) != 0);
+            tc::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, kIdescCH, (kb | k) != 0);
           tc::mma_commit(&ctl.empty[s]);
         }
         if (!ok) break;
@@ -742,7 +747,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
     const int m_lo = y * p.rows_per_rep + (q * 32) % p.rows_per_rep - p.lane_shift;
     const bool warp_live = m_lo + 31 >= 0 && m_lo < p.M;
     const float kNaN = __int_as_float(0x7FC00000);
-    const int cols = kChunk / p.R;
+    const int cols = CH / p.R;
     const int jb = rep * cols;
     const int qstep = p.rows_per_rep / 32;
     constexpr int kSub = KT <= 4 ? 4 : 2;
@@ -750,9 +755,9 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
 #pragma unroll
     for (int j = 0; j < kSub; ++j) sub[j].reset();
     for (int c = 0;; ++c) {
-      const int a = c % kAcc;
+      const int a = c % kNAcc;
       int okw = 1;
-      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (c / kAcc) & 1, abort_flag) ? 1 : 0;
+      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (c / kNAcc) & 1, abort_flag) ? 1 : 0;
       okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
       if (!epilogue_all(okw != 0)) {  // uniform: every epilogue warp leaves together
         if (lane == 0) { *abort_flag = 1; record_error(p.err, kDevErrTimeout); }
@@ -764,13 +769,13 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
       const int dc = desc_chunk[c % kDescRing];
       const int j = dc & 0x7FFFFFFF;
       const bool last = dc < 0;
-      const int64_t cbase = ((int64_t)tile * cpt + j) * kChunk;
-      const int64_t cend = min(n, cbase + kChunk);
+      const int64_t cbase = ((int64_t)tile * cpt + j) * CH;
+      const int64_t cend = min(n, cbase + CH);
       for (int j0 = jb; j0 < jb + cols && warp_live; j0 += 32) {
         const int64_t base = cbase + j0;
         if (base >= cend) break;
         uint32_t v[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kChunk + j0), v);
+        tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * CH + j0), v);
         tc::tmem_ld_wait();
         const int lim = (int)min((int64_t)32, cend - base);
         uint32_t ties = 0;
@@ -831,340 +836,33 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
   }
 }
 
-// ---------------------------------------------------------------- small batches
-// Variant for at most 32 hidden vectors and tiles of a multiple of 128 rows.
-// The operands swap roles: the 128-row vocabulary chunk is the MMA's M side
-// and the hidden vectors its N side (N = 16 or 32), so a chunk costs 128 x N
-// products on the tensor cores instead of 128 x 128 (the hidden rows are no
-// longer padded or copied to 128 lanes), and u takes N x r instead of 128 x r
-// of shared memory, which goes to the A ring. Tiles are claimed as in the
-// dynamic kernel. Epilogue: each thread reads its vocabulary row's N scores
-// from TMEM and writes them transposed into shared memory (double-buffered);
-// then P = 128 / N threads per hidden vector scan N rows each of the chunk
-// with the same register top-k, and at a tile end the P lists of a hidden
-// vector meet in shared memory.
-constexpr int kSmallN = 32;        // largest N of the small-batch kernel
-constexpr int kSPad = 4;           // fp32 padding per transposed row (bank spread)
-constexpr int kSRow = kChunk + kSPad;
-
-template <int KT, int N>
-__global__ void __launch_bounds__(kThreads, 1)
-local_topk_tcs_kernel(const __grid_constant__ CUtensorMap amap,
-                      const __grid_constant__ CUtensorMap umap, const Params p) {
-  extern __shared__ uint8_t dsmem_raw[];
-  __shared__ SharedCtl ctl;
-  __shared__ int desc_tile[kDescRing], desc_chunk[kDescRing];
-  uint8_t* dsmem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  constexpr int kUBox = N * 128;  // bytes of one u box (N rows x 64 bf16)
-  constexpr int P = kChunk / N;   // threads per hidden vector in the scan
-  const int kblocks = (p.r + kKBlock - 1) / kKBlock;
-  uint8_t* u_s = dsmem;
-  uint8_t* stage_s = dsmem + (size_t)kblocks * kUBox;  // 1024-aligned: kUBox is a multiple of 2 KB
-  float* S = reinterpret_cast<float*>(stage_s + (size_t)p.stages * kStageBytes);  // [2][N][kSRow]
-  float2* xchg = reinterpret_cast<float2*>(S + 2 * N * kSRow);                  // [128][KT]
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int y = blockIdx.y;
-  const int NS = p.stages;
-  const int64_t n = p.n, T = p.T;
-  const int cpt = (int)(T / kChunk);
-  int* counter = p.tile_tickets + y;
-  volatile int* abort_flag = &ctl.abort;
-  constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kChunk, N);
-  const int nchain = min(kblocks, kChunk / N);  // accumulation chains per chunk
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      tc::mbar_init(&ctl.full[s], 1);
-      tc::mbar_init(&ctl.empty[s], 1);
-    }
-    tc::mbar_init(&ctl.ufull, 1);
-    for (int a = 0; a < kAcc; ++a) {
-      tc::mbar_init(&ctl.acc_full[a], 1);
-      tc::mbar_init(&ctl.acc_empty[a], 4);
-    }
-    ctl.abort = 0;
-    tc::fence_mbar_init();
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(&ctl.tmem_base, kTmemCols);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
-  cta_sync();
-  tc::fence_after_sync();
-  const uint32_t tmem = ctl.tmem_base;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tc::prefetch_tmap(&amap);
-      tc::prefetch_tmap(&umap);
-      uint32_t it = 0;
-      int c = 0;
-      const int grp = min(min(4, NS), kblocks);
-      bool ok = true, u_loaded = false;
-      auto load_u = [&]() {
-        pdl_wait();  // u is written by the previous kernel
-        tc::mbar_arrive_expect_tx(&ctl.ufull, (uint32_t)(kblocks * kUBox));
-        for (int ub = 0; ub < kblocks; ++ub)
-          tc::tma_load_2d(u_s + (size_t)ub * kUBox, &umap, &ctl.ufull, ub * kKBlock, y * N);
-        u_loaded = true;
-      };
-      int64_t tile = blockIdx.x < p.tiles ? (int64_t)blockIdx.x : -1;
-      int64_t next = -1;
-      while (ok) {
-        if (tile >= 0 && u_loaded && next < 0) next = (int64_t)p.G + atomicAdd(counter, 1);
-        const int slot = c % kDescRing;
-        if (tile < 0 || tile >= p.tiles) {  // no more work: an end marker through the ring
-          const int s = (int)(it % NS);
-          if (it >= (uint32_t)NS && !tc::mbar_wait(&ctl.empty[s], ((it / NS) & 1) ^ 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          desc_tile[slot] = -1;
-          tc::mbar_arrive(&ctl.full[s]);
-          ++it;
-          break;
-        }
-        for (int j = 0; j < cpt && ok; ++j) {
-          const int64_t gc = tile * cpt + j;
-          if (gc * kChunk >= n) break;
-          const bool last = j == cpt - 1 || (gc + 1) * kChunk >= n;
-          desc_tile[c % kDescRing] = (int)tile;
-          desc_chunk[c % kDescRing] = j | (last ? (int)0x80000000 : 0);
-          for (int kb0 = 0; kb0 < kblocks && ok; kb0 += grp) {
-            const int gcount = min(grp, kblocks - kb0);
-            if (!u_loaded && it + (uint32_t)gcount > (uint32_t)NS) load_u();
-            for (int g2 = 0; g2 < gcount; ++g2) {
-              const uint32_t itg = it + (uint32_t)g2;
-              if (itg >= (uint32_t)NS &&
-                  !tc::mbar_wait(&ctl.empty[itg % NS], ((itg / NS) & 1) ^ 1, abort_flag)) {
-                ok = false;
-                break;
-              }
-            }
-            if (!ok) break;
-            for (int g2 = 0; g2 < gcount; ++g2, ++it) {
-              const int s = (int)(it % NS);
-              tc::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
-              tc::tma_load_2d(stage_s + (size_t)s * kStageBytes, &amap, &ctl.full[s],
-                              (kb0 + g2) * kKBlock, (int)(gc * kChunk));
-            }
-            if (!u_loaded && (it >= (uint32_t)NS || (j == cpt - 1 && kb0 + gcount == kblocks)))
-              load_u();
-          }
-          ++c;
-        }
-        if (!u_loaded) load_u();
-        if (tile >= 0 && next < 0) next = (int64_t)p.G + atomicAdd(counter, 1);
-        tile = next;
-        next = -1;
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        record_error(p.err, kDevErrTimeout);
-      }
-      pdl_trigger();
-      if (*abort_flag) {
-        const uint32_t first = it > (uint32_t)NS ? it - NS : 0;
-        for (uint32_t jq = first; jq < it; ++jq) {
-          const long long t0 = clock64();
-          while (!tc::mbar_try_wait(&ctl.full[jq % NS], (jq / NS) & 1) &&
-                 clock64() - t0 < tc::kWaitCycles) {
-          }
-        }
-        const long long t0 = clock64();
-        while (u_loaded && !tc::mbar_try_wait(&ctl.ufull, 0) && clock64() - t0 < tc::kWaitCycles) {
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = tc::mbar_wait(&ctl.ufull, 0, abort_flag);
-      uint32_t it = 0;
-      for (int c = 0; ok; ++c) {
-        const int a = c % kAcc;
-        int s = (int)(it % NS);
-        if (!tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag)) { ok = false; break; }
-        if (!tc::mbar_wait(&ctl.acc_empty[a], ((c / kAcc) & 1) ^ 1, abort_flag)) { ok = false; break; }
-        if (desc_tile[c % kDescRing] < 0) {  // end marker (after the slot is free, as above)
-          tc::mbar_arrive(&ctl.acc_full[a]);
-          break;
-        }
-        tc::fence_after_sync();
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          s = (int)(it % NS);
-          if (kb > 0 && !tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag)) { ok = false; break; }
-          tc::fence_after_sync();
-          // D[vocabulary row, hidden vector] += A chunk (M side) x u (N side); the
-          // K-blocks feed nchain separate column blocks (shorter dependent chains)
-          const uint32_t d = tmem + a * kChunk + (uint32_t)((kb % nchain) * N);
-          const uint64_t adesc = tc::sw128_kmajor_desc(tc::smem_addr(stage_s + (size_t)s * kStageBytes));
-          const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_addr(u_s + (size_t)kb * kUBox));
-          const int nk = min(4, (p.r - kb * kKBlock + 15) / 16);
-          for (int k = 0; k < nk; ++k)
-            tc::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, kIdescS, (kb >= nchain || k > 0) ? 1u : 0u);
-          tc::mma_commit(&ctl.empty[s]);
-        }
-        if (!ok) break;
-        tc::mma_commit(&ctl.acc_full[a]);
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        record_error(p.err, kDevErrTimeout);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    pdl_wait();
-    const int q = warp & 3;             // TMEM lane quadrant this warp may read
-    const int et = (warp - 2) * 32 + lane;  // epilogue thread 0..127
-    const int ml = et % N, part = et / N;
-    const int m = y * N + ml;
-    const bool valid = m < p.M;
-    const float kNaN = __int_as_float(0x7FC00000);
-    constexpr int kSub = KT <= 4 ? 4 : 2;
-    RegList<KT, true> sub[kSub];
-#pragma unroll
-    for (int j = 0; j < kSub; ++j) sub[j].reset();
-    for (int c = 0;; ++c) {
-      const int a = c % kAcc;
-      int okw = 1;
-      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (c / kAcc) & 1, abort_flag) ? 1 : 0;
-      okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
-      if (!epilogue_all(okw != 0)) {
-        if (lane == 0) { *abort_flag = 1; record_error(p.err, kDevErrTimeout); }
-        break;
-      }
-      tc::fence_after_sync();
-      const int tile = desc_tile[c % kDescRing];
-      if (tile < 0) break;
-      const int dc = desc_chunk[c % kDescRing];
-      const int j = dc & 0x7FFFFFFF;
-      const bool last = dc < 0;
-      const int64_t cbase = ((int64_t)tile * cpt + j) * kChunk;
-      const int64_t cend = min(n, cbase + kChunk);
-      // this thread's vocabulary row: its N scores, transposed into S[buf]
-      float* Sb = S + (c & 1) * N * kSRow;
-      {
-        float acc[N];
-#pragma unroll
-        for (int col = 0; col < N; ++col) acc[col] = 0.f;
-        for (int ch = 0; ch < nchain; ++ch) {  // sum the chains' column blocks
-          uint32_t v[N];
-          const uint32_t taddr =
-              tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kChunk + ch * N);
-          if constexpr (N == 16) tc::tmem_ld16(taddr, v); else tc::tmem_ld32(taddr, v);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int col = 0; col < N; ++col) acc[col] += __uint_as_float(v[col]);
-        }
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&ctl.acc_empty[a]);  // the accumulator is free again
-#pragma unroll
-        for (int col = 0; col < N; ++col) Sb[col * kSRow + q * 32 + lane] = acc[col];
-      }
-      named_sync(1, 128);
-      // scan rows [part*N, part*N + N) of the chunk for hidden vector ml
-      {
-        const float4* src = reinterpret_cast<const float4*>(Sb + ml * kSRow + part * N);
-        const int64_t base = cbase + part * N;
-        float x[N];
-#pragma unroll
-        for (int i = 0; i < N / 4; ++i) {
-          const float4 f = src[i];
-          x[4 * i] = f.x; x[4 * i + 1] = f.y; x[4 * i + 2] = f.z; x[4 * i + 3] = f.w;
-        }
-        uint32_t ties = 0;
-#pragma unroll
-        for (int i = 0; i < N; ++i) {
-          const bool live = valid && base + i < cend;
-          const bool t = sub[i % kSub].push_fast(live ? x[i] : kNaN, (int32_t)(base + i));
-          ties |= (t ? 1u : 0u) << i;
-        }
-        for (uint32_t t = ties; t; t &= t - 1) {  // rare: exact ties, re-read from S
-          const int i = __ffs(t) - 1;
-          sub[0].push_exact(Sb[ml * kSRow + part * N + i], (int32_t)(base + i), p.token_ids, n);
-        }
-      }
-      if (last) {  // the tile is complete: the P lists of each hidden vector meet
-        RegList<KT, true> Lst = sub[0];
-#pragma unroll
-        for (int jj = 1; jj < kSub; ++jj) Lst.absorb(sub[jj], p.token_ids, n);
-#pragma unroll
-        for (int jj = 0; jj < KT; ++jj)
-          xchg[et * KT + jj] = make_float2(Lst.s[jj], __int_as_float(Lst.k[jj]));
-        named_sync(1, 128);
-        if (part == 0) {
-          for (int o = 1; o < P; ++o) {
-#pragma unroll
-            for (int jj = 0; jj < KT; ++jj) {
-              const float2 e = xchg[(o * N + ml) * KT + jj];
-              Lst.push_exact(e.x == -INFINITY ? kNaN : e.x, __float_as_int(e.y), p.token_ids, n);
-            }
-          }
-          if (valid)
-            write_tile<KT>(p, m, tile,
-                           (int)min((int64_t)KT, min(n, (int64_t)(tile + 1) * T) - (int64_t)tile * T),
-                           Lst, true);
-        }
-        named_sync(1, 128);
-#pragma unroll
-        for (int jj = 0; jj < kSub; ++jj) sub[jj].reset();
-      }
-    }
-  }
-
-  tc::fence_before_sync();
-  cta_sync();
-  if (warp == 1) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
 // ---------------------------------------------------------------- host side
-template <int KT, int N>
-cudaError_t launch_small(const CUtensorMap& amap, const CUtensorMap& umap, const Params& p,
-                         size_t smem, cudaStream_t s) {
-  static int smem_set[64] = {0};
-  cudaError_t e = ensure_dynamic_smem(local_topk_tcs_kernel<KT, N>, smem, smem_set);
-  if (e != cudaSuccess) return e;
-  return launch_kernel(true, local_topk_tcs_kernel<KT, N>, dim3(p.G, 1), dim3(kThreads), smem, s,
-                       amap, umap, p);
-}
-
-template <int KT>
-cudaError_t launch_kt_small(const CUtensorMap& amap, const CUtensorMap& umap, const Params& p,
-                            int N, size_t smem, cudaStream_t s) {
-  return N == 16 ? launch_small<KT, 16>(amap, umap, p, smem, s)
-                 : launch_small<KT, 32>(amap, umap, p, smem, s);
-}
-
-// LMHEAD_K4_SMALL = 0 keeps small batches on the 128-lane kernel (measurements only).
-bool small_kernel_enabled() {
+// LMHEAD_K4_CHUNK = 128 keeps 128-row MMAs for every tile (measurements only).
+bool chunk256_enabled() {
   static int v = -1;
   if (v < 0) {
-    const char* e = getenv("LMHEAD_K4_SMALL");
-    v = (e && e[0] == '0') ? 0 : 1;
+    const char* e = getenv("LMHEAD_K4_CHUNK");
+    v = (e && atoi(e) == 128) ? 0 : 1;
   }
   return v == 1;
 }
 
+template <int KT, int CH>
+cudaError_t launch_dyn(const CUtensorMap& amap, const CUtensorMap& umap, const Params& p, int HC,
+                       size_t smem, cudaStream_t s) {
+  static int smem_set_dyn[64] = {0};
+  cudaError_t e = ensure_dynamic_smem(local_topk_tc_dyn_kernel<KT, CH>, smem, smem_set_dyn);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(true, local_topk_tc_dyn_kernel<KT, CH>, dim3(p.G, HC), dim3(kThreads), smem,
+                       s, amap, umap, p);
+}
+
 template <int KT>
 cudaError_t launch_kt(const CUtensorMap& amap, const CUtensorMap& umap, const Params& p, int HC,
-                      size_t smem, cudaStream_t s) {
-  if (p.T % kChunk == 0) {
-    static int smem_set_dyn[64] = {0};
-    cudaError_t e = ensure_dynamic_smem(local_topk_tc_dyn_kernel<KT>, smem, smem_set_dyn);
-    if (e != cudaSuccess) return e;
-    return launch_kernel(true, local_topk_tc_dyn_kernel<KT>, dim3(p.G, HC), dim3(kThreads), smem, s,
-                         amap, umap, p);
-  }
+                      size_t smem, int ch, cudaStream_t s) {
+  if (p.T % kChunk == 0)
+    return ch == 256 ? launch_dyn<KT, 256>(amap, umap, p, HC, smem, s)
+                     : launch_dyn<KT, 128>(amap, umap, p, HC, smem, s);
   static int smem_set[64] = {0};
   cudaError_t e = ensure_dynamic_smem(local_topk_tc_kernel<KT>, smem, smem_set);
   if (e != cudaSuccess) return e;
@@ -1213,38 +911,13 @@ cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t
   const int kblocks = (r + kKBlock - 1) / kKBlock;
   const size_t budget = 232448 - 2048;  // opt-in shared memory minus static + alignment slack
   const size_t xchg_bytes = (size_t)kHid * 8 * sizeof(float2);
-  if (T % kChunk == 0 && M <= kSmallN && small_kernel_enabled()) {
-    // small batch: hidden vectors on the MMA's N side (local_topk_tcs_kernel)
-    const int N = M <= 16 ? 16 : 32;
-    const size_t u_small = (size_t)kblocks * N * 128;
-    const size_t s_bytes = (size_t)2 * N * kSRow * sizeof(float);
-    int st = (int)((budget - 1024 - u_small - s_bytes - xchg_bytes) / kStageBytes);
-    if (st > kMaxStages) st = kMaxStages;
-    if (st < 2) return cudaErrorInvalidValue;
-    p.stages = st;
-    p.R = 1;
-    p.rows_per_rep = N;
-    p.lane_shift = 0;
-    p.out_ids = out_ids;
-    p.out_scores = out_scores;
-    p.partials = static_cast<float2*>(partials);
-    p.tile_tickets = tile_tickets;
-    p.err = err;
-    CUtensorMap amap_s, umap_s;
-    if (!make_bf16_map(&amap_s, A, (uint64_t)n, (uint64_t)r, kChunk, kKBlock) ||
-        !make_bf16_map(&umap_s, u, (uint64_t)M, (uint64_t)r, N, kKBlock))
-      return cudaErrorInvalidValue;
-    const size_t smem_s = 1024 + u_small + (size_t)st * kStageBytes + s_bytes + xchg_bytes;
-    switch (k_tile) {
-      case 1: return launch_kt_small<1>(amap_s, umap_s, p, N, smem_s, s);
-      case 2: return launch_kt_small<2>(amap_s, umap_s, p, N, smem_s, s);
-      case 4: return launch_kt_small<4>(amap_s, umap_s, p, N, smem_s, s);
-      case 8: return launch_kt_small<8>(amap_s, umap_s, p, N, smem_s, s);
-      default: return cudaErrorInvalidValue;
-    }
-  }
   const size_t u_bytes = (size_t)kblocks * kStageBytes;
-  int stages = (int)((budget - 1024 - u_bytes - xchg_bytes) / kStageBytes);
+  // tiles of a multiple of 256 rows: one MMA covers 256 rows (N = 256). The
+  // tensor pipe takes about the same time per MMA at N = 128 as at N = 256,
+  // so the wider MMA halves the tensor time per byte of A.
+  const int ch = (T % 256 == 0 && chunk256_enabled()) ? 256 : kChunk;
+  const size_t st_bytes = (size_t)ch * 128;
+  int stages = (int)((budget - 1024 - u_bytes - xchg_bytes) / st_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return cudaErrorInvalidValue;
   p.stages = stages;
@@ -1257,16 +930,16 @@ cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t
   p.tile_tickets = tile_tickets;
   p.err = err;
   CUtensorMap amap, umap;
-  if (!make_bf16_map(&amap, A, (uint64_t)n, (uint64_t)r, kChunk, kKBlock) ||
+  if (!make_bf16_map(&amap, A, (uint64_t)n, (uint64_t)r, ch, kKBlock) ||
       !make_bf16_map(&umap, u, (uint64_t)M, (uint64_t)r, p.rows_per_rep, kKBlock))
     return cudaErrorInvalidValue;
   const int HC = (M + p.rows_per_rep - 1) / p.rows_per_rep;
-  const size_t smem = 1024 + u_bytes + (size_t)stages * kStageBytes + xchg_bytes;
+  const size_t smem = 1024 + u_bytes + (size_t)stages * st_bytes + xchg_bytes;
   switch (k_tile) {
-    case 1: return launch_kt<1>(amap, umap, p, HC, smem, s);
-    case 2: return launch_kt<2>(amap, umap, p, HC, smem, s);
-    case 4: return launch_kt<4>(amap, umap, p, HC, smem, s);
-    case 8: return launch_kt<8>(amap, umap, p, HC, smem, s);
+    case 1: return launch_kt<1>(amap, umap, p, HC, smem, ch, s);
+    case 2: return launch_kt<2>(amap, umap, p, HC, smem, ch, s);
+    case 4: return launch_kt<4>(amap, umap, p, HC, smem, ch, s);
+    case 8: return launch_kt<8>(amap, umap, p, HC, smem, ch, s);
     default: return cudaErrorInvalidValue;
   }
 }
