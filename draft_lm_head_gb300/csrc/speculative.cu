@@ -12,14 +12,16 @@
 // candidate-supported distribution, zero outside the row's candidates) and
 // stop; when every draft is accepted, draw a bonus token from p_Kd. Draws
 // use the inverse CDF in vocabulary order with one caller-supplied uniform.
-// One CTA per chain: the candidates of the rejected position go into a
-// shared-memory hash table, warps sum the residual over contiguous runs of
-// the vocabulary with coalesced loads, and a scan of the run sums places the
-// draw.
+// One 8-CTA cluster per chain: every CTA takes the accept decisions, puts
+// the candidates of the rejected position into a shared-memory hash table and
+// sums the residual over its eighth of the vocabulary (warps over contiguous
+// runs, coalesced loads); the CTA totals meet in distributed shared memory and
+// the CTA holding the draw places it with a scan of its run sums.
 #include <math.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_util.cuh"
 
 namespace lmhead {
 namespace {
@@ -116,6 +118,7 @@ draft_select_kernel(const float* __restrict__ q, const int32_t* __restrict__ ids
 
 // ---------------------------------------------------------------- K9
 constexpr int kVerThreads = 1024;
+constexpr int kVerCluster = 8;     // CTAs per chain (the vocabulary is split over them)
 constexpr int kHashSlots = 8192;  // >= 2 x kSelectMaxK
 
 __device__ __forceinline__ uint32_t hash_slot(int32_t id) {
@@ -124,24 +127,31 @@ __device__ __forceinline__ uint32_t hash_slot(int32_t id) {
 
 // Inverse-CDF draw over w_v = max(0, p_v - q(v)) (q from the hash table, or
 // none when use_q is false): the smallest v whose running sum exceeds u * W.
-// The vocabulary is read in chunks of 32 consecutive entries (one coalesced
-// load per warp); warp w owns a contiguous run of chunks and sums it (lane
-// partials, then one warp reduction). Warp offsets chain the warp totals in
-// warp order, so every warp's interval [off_w, off_{w+1}) holds exactly the
-// targets it owns. The owning warp walks its run again in blocks of 32
-// chunks (one chunk sum per lane, a scan over them) and, in the crossing
-// chunk, takes the first entry whose running sum passes the target. Where
-// rounding keeps a walk from crossing, or u * W rounds up to W, the last
-// positive weight of the run (of the vocabulary) is taken.
-// W == 0 falls back to p itself. Returns the token on every thread.
+// The vocabulary is split over the kVerCluster CTAs of the chain's cluster
+// (CTA `rank` owns a contiguous run of 32-entry chunks) and, inside a CTA,
+// over its warps. Every warp sums its run (coalesced loads, lane partials,
+// one warp reduction); CTA totals are summed in warp order and exchanged
+// through distributed shared memory, so every CTA sees the same CTA totals
+// and the same W, and the target u * W falls into exactly one CTA's interval
+// (CTA offsets chain the totals in rank order). Inside that CTA the warp
+// whose interval holds the target walks its run again in blocks of 32 chunks
+// (one chunk sum per lane, a scan over them) and, in the crossing chunk,
+// takes the first entry whose running sum passes the target. Where rounding
+// keeps a walk from crossing, or u * W rounds up to W, the last positive
+// weight of the run (of the vocabulary) is taken. W == 0 falls back to p
+// itself. Returns the token in the CTA that drew it and -1 in the others.
 __device__ int residual_draw(const float* __restrict__ prow, int64_t n, bool use_q,
                              const int32_t* tkey, const float* tval, float u, float* wtot,
-                             int* s_tok) {
+                             int* s_tok, float* cta_tot, int rank) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int kWarps = kVerThreads / 32;
   const int64_t nch = (n + 31) / 32;
-  const int64_t cpw = (nch + kWarps - 1) / kWarps;
-  const int64_t c0 = warp * cpw, c1 = c0 + cpw < nch ? c0 + cpw : nch;
+  const int64_t cpc = (nch + kVerCluster - 1) / kVerCluster;  // chunks per CTA
+  const int64_t s0 = rank * cpc < nch ? rank * cpc : nch;
+  const int64_t s1 = s0 + cpc < nch ? s0 + cpc : nch;
+  const int64_t cpw = (s1 - s0 + kWarps - 1) / kWarps;
+  const int64_t c0 = s0 + warp * cpw < s1 ? s0 + warp * cpw : s1;
+  const int64_t c1 = c0 + cpw < s1 ? c0 + cpw : s1;
   auto weight = [&](int64_t v, bool sub) -> float {
     if (v >= n) return 0.f;
     float w = prow[v];
@@ -165,21 +175,32 @@ __device__ int residual_draw(const float* __restrict__ prow, int64_t n, bool use
     if (lane == 0) wtot[warp] = run;
     if (threadIdx.x == 0) *s_tok = -1;
     cta_sync();
-    float off = 0.f, total = 0.f;
+    float woff = 0.f, ctot = 0.f;  // this warp's offset inside the CTA, the CTA total
     for (int w = 0; w < kWarps; ++w) {
-      if (w == warp) off = total;
-      total += wtot[w];
+      if (w == warp) woff = ctot;
+      ctot += wtot[w];
     }
-    const float hi = warp + 1 < kWarps ? off + wtot[warp] : total;
-    if (!(total > 0.f)) {  // (p - q)+ vanishes: draw from p
-      cta_sync();
-      continue;
+    if (threadIdx.x == 0) *cta_tot = ctot;
+    tc::cluster_sync();  // every CTA total is published
+    float coff = 0.f, total = 0.f;
+    int last_pos_rank = -1;
+    const uint32_t tot_addr = tc::smem_addr(cta_tot);
+    for (int rr = 0; rr < kVerCluster; ++rr) {
+      const float tr = tc::ld_cluster_f32(tc::map_to_rank(tot_addr, (uint32_t)rr));
+      if (rr == rank) coff = total;
+      if (tr > 0.f) last_pos_rank = rr;
+      total += tr;
     }
+    tc::cluster_sync();  // the totals have been read before any CTA moves on or exits
+    if (!(total > 0.f)) continue;  // (p - q)+ vanishes: draw from p (same in every CTA)
     const float target = u * total;
-    if (off <= target && target < hi) {
-      // walk the run in blocks of 32 chunks: lane L sums chunk b + L (its
-      // loads are independent), a scan over the 32 chunk sums and a ballot
-      // find the crossing chunk, a scan over its 32 lanes the entry
+    const float chi = rank + 1 < kVerCluster ? coff + ctot : total;
+    const bool past_end = !(target < total);  // u * W rounded up to W
+    const bool mine = (coff <= target && target < chi) || (past_end && rank == last_pos_rank);
+    if (!mine) return -1;
+    const float off = coff + woff;
+    const float hi = warp + 1 < kWarps ? off + wtot[warp] : chi;
+    if (!past_end && off <= target && target < hi) {
       float acc = off;
       int64_t pick = -1, last_pos = -1;
       for (int64_t b = c0; b < c1 && pick < 0; b += 32) {
@@ -222,7 +243,7 @@ __device__ int residual_draw(const float* __restrict__ prow, int64_t n, bool use
       if (lane == 0) *s_tok = (int)pick;
     }
     cta_sync();
-    if (*s_tok < 0 && wtot[warp] > 0.f) {  // target at or past W: the last positive weight
+    if (*s_tok < 0 && wtot[warp] > 0.f) {  // target at or past this CTA's end: last positive weight
       int64_t last_pos = -1;
       for (int64_t c = c1 - 1; c >= c0 && last_pos < 0; --c) {
         const uint32_t pos = __ballot_sync(0xFFFFFFFFu, weight(c * 32 + lane, sub) > 0.f);
@@ -235,10 +256,11 @@ __device__ int residual_draw(const float* __restrict__ prow, int64_t n, bool use
     cta_sync();
     return tok;
   }
-  return (int)(n - 1);
+  // p itself sums to zero (invalid input): the last entry, drawn by the last CTA
+  return rank == kVerCluster - 1 ? (int)(n - 1) : -1;
 }
 
-__global__ void __launch_bounds__(kVerThreads)
+__global__ void __cluster_dims__(kVerCluster, 1, 1) __launch_bounds__(kVerThreads, 1)
 verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_t* __restrict__ x,
                     const int32_t* __restrict__ cand_ids, const float* __restrict__ cand_q, int K,
                     const float* __restrict__ r, const float* __restrict__ u,
@@ -248,13 +270,19 @@ verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_
   int32_t* tkey = vsm;                                          // [kHashSlots]
   float* tval = reinterpret_cast<float*>(vsm + kHashSlots);     // [kHashSlots]
   __shared__ float wtot[kVerThreads / 32];
+  __shared__ float cta_tot;
   __shared__ int s_hit, s_tok;
-  const int b = blockIdx.x;
+  const int b = blockIdx.y;
+  const int rank = (int)tc::cluster_ctarank();
   const float* pb = p + (size_t)b * (Kd + 1) * n;
   int32_t* ob = out_tokens + (size_t)b * (Kd + 1);
   pdl_wait();  // the candidate lists may come from the previous kernel
-  for (int i = threadIdx.x; i <= Kd; i += kVerThreads) ob[i] = -1;
-  for (int t = 0; t < Kd; ++t) {
+  // CTA 0 writes the accepted drafts and the count; the CTA that draws the
+  // last token writes it (after the cluster barriers inside the draw, so
+  // after CTA 0's initialisation below)
+  if (rank == 0)
+    for (int i = threadIdx.x; i <= Kd; i += kVerThreads) ob[i] = -1;
+  for (int t = 0; t < Kd; ++t) {  // every CTA takes the same decisions
     const int32_t xt = x[(size_t)b * Kd + t];
     const int32_t* ci = cand_ids + ((size_t)b * Kd + t) * K;
     const float* cq = cand_q + ((size_t)b * Kd + t) * K;
@@ -265,7 +293,7 @@ verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_
     cta_sync();
     const int hit = s_hit;
     if (hit >= K || xt < 0 || (int64_t)xt >= n) {  // not a candidate of its row
-      if (threadIdx.x == 0) {
+      if (rank == 0 && threadIdx.x == 0) {
         record_error(err, kDevErrBadId);
         out_count[b] = -1;
       }
@@ -274,7 +302,7 @@ verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_
     const float px = pb[(size_t)t * n + xt];
     const float qx = cq[hit];
     if (r[(size_t)b * Kd + t] < px / qx) {
-      if (threadIdx.x == 0) ob[t] = xt;
+      if (rank == 0 && threadIdx.x == 0) ob[t] = xt;
       continue;
     }
     // rejected: the residual (p_t - q_t)+ over the vocabulary
@@ -295,18 +323,18 @@ verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_
     }
     cta_sync();
     const int tok = residual_draw(pb + (size_t)t * n, n, true, tkey, tval,
-                                  u[(size_t)b * (Kd + 1) + t], wtot, &s_tok);
+                                  u[(size_t)b * (Kd + 1) + t], wtot, &s_tok, &cta_tot, rank);
     if (threadIdx.x == 0) {
-      ob[t] = tok;
-      out_count[b] = t;
+      if (tok >= 0) ob[t] = tok;
+      if (rank == 0) out_count[b] = t;
     }
     return;
   }
   const int tok = residual_draw(pb + (size_t)Kd * n, n, false, tkey, tval,
-                                u[(size_t)b * (Kd + 1) + Kd], wtot, &s_tok);
+                                u[(size_t)b * (Kd + 1) + Kd], wtot, &s_tok, &cta_tot, rank);
   if (threadIdx.x == 0) {
-    ob[Kd] = tok;
-    out_count[b] = Kd;
+    if (tok >= 0) ob[Kd] = tok;
+    if (rank == 0) out_count[b] = Kd;
   }
 }
 
@@ -336,8 +364,8 @@ cudaError_t launch_verify_chain(const float* p, int64_t n, int B, int Kd, const 
   static int smem_set[64] = {0};
   cudaError_t e = ensure_dynamic_smem(verify_chain_kernel, smem, smem_set);
   if (e != cudaSuccess) return e;
-  return launch_kernel(true, verify_chain_kernel, dim3(B), dim3(kVerThreads), smem, s, p, n, Kd, x,
-                       cand_ids, cand_q, K, r, u, out_tokens, out_count, err);
+  return launch_kernel(true, verify_chain_kernel, dim3(kVerCluster, B), dim3(kVerThreads), smem, s,
+                       p, n, Kd, x, cand_ids, cand_q, K, r, u, out_tokens, out_count, err);
 }
 
 }  // namespace lmhead
