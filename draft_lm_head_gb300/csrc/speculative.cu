@@ -4,7 +4,7 @@
 // dynamic draft tree, Expansion Phase): per row (one node of the draft tree)
 // the k_sel most likely draft tokens by q (ties: smaller vocabulary id) with
 // their path values parent_value * q, and optionally one token drawn from q
-// by the Gumbel-max construction on caller-supplied uniforms. One CTA per row.
+// by the Gumbel-max construction on caller-supplied uniforms. One warp per row.
 //
 // K9 chain verification ("Speculative decoding and EAGLE", exactness rule):
 // for each drafted token x_t, accept if r_t < p_t(x_t) / q_t(x_t); otherwise
@@ -26,18 +26,16 @@
 namespace lmhead {
 namespace {
 
-constexpr int kSelThreads = 256;
+constexpr int kSelThreads = 64;  // two rows (warps) per CTA
 
 // a beats b: larger q, then smaller id
 __device__ __forceinline__ bool q_beats(float qa, int32_t ia, float qb, int32_t ib) {
   return qa > qb || (qa == qb && ia < ib);
 }
 
-// Block-wide arg-best over (key, id) pairs: larger key wins, then smaller id.
-// Every thread returns the winner. sh: 2 * kSelThreads / 32 words.
-__device__ __forceinline__ void block_best(float& key, int32_t& id, int& who, float* shk, int* shi,
-                                           int* shw) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+// Warp-wide arg-best over (key, id) pairs: larger key wins, then smaller id;
+// `who` travels with the winner. Every lane returns the winner.
+__device__ __forceinline__ void warp_best(float& key, int32_t& id, int& who) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const float ok = __shfl_xor_sync(0xFFFFFFFFu, key, off);
@@ -45,62 +43,80 @@ __device__ __forceinline__ void block_best(float& key, int32_t& id, int& who, fl
     const int ow = __shfl_xor_sync(0xFFFFFFFFu, who, off);
     if (q_beats(ok, oi, key, id)) { key = ok; id = oi; who = ow; }
   }
-  if (lane == 0) { shk[warp] = key; shi[warp] = id; shw[warp] = who; }
-  cta_sync();
-  key = shk[0]; id = shi[0]; who = shw[0];
-  for (int w = 1; w < nw; ++w)
-    if (q_beats(shk[w], shi[w], key, id)) { key = shk[w]; id = shi[w]; who = shw[w]; }
-  cta_sync();  // the scratch is reused by the next call
 }
 
+// One warp per row: every lane keeps the sorted top KT of its strided share
+// of the row in registers (branch-free insertion: the comparisons against a
+// sorted list are monotone, so each slot takes its own value, its upper
+// neighbour's or the new one); k_sel rounds of a warp arg-best over the list
+// heads then pick the outputs in order, the winning lane popping its head.
 template <int KT>
 __global__ void __launch_bounds__(kSelThreads)
-draft_select_kernel(const float* __restrict__ q, const int32_t* __restrict__ ids, int K, int k_sel,
-                    const float* __restrict__ parent_value, const float* __restrict__ uniforms,
-                    int32_t* __restrict__ top_ids, float* __restrict__ top_q,
-                    float* __restrict__ top_value, int32_t* __restrict__ sample_id,
-                    float* __restrict__ sample_q) {
-  __shared__ float lq[kSelThreads][KT];
-  __shared__ int32_t li[kSelThreads][KT];
-  __shared__ float shk[kSelThreads / 32];
-  __shared__ int shi[kSelThreads / 32], shw[kSelThreads / 32];
-  const int tid = threadIdx.x;
-  const size_t row = (size_t)blockIdx.x * K;
+draft_select_kernel(const float* __restrict__ q, const int32_t* __restrict__ ids, int M, int K,
+                    int k_sel, const float* __restrict__ parent_value,
+                    const float* __restrict__ uniforms, int32_t* __restrict__ top_ids,
+                    float* __restrict__ top_q, float* __restrict__ top_value,
+                    int32_t* __restrict__ sample_id, float* __restrict__ sample_q) {
+  const int lane = threadIdx.x & 31;
+  const int m = blockIdx.x * (kSelThreads / 32) + (threadIdx.x >> 5);
   pdl_wait();  // q comes from the previous kernel
-  // this thread's sorted top-KT of its strided share, kept in shared memory
-  for (int i = 0; i < KT; ++i) { lq[tid][i] = -INFINITY; li[tid][i] = 0x7FFFFFFF; }
-  float gk = -INFINITY;  // Gumbel-max: best perturbed log q of this thread
+  if (m >= M) return;
+  const size_t row = (size_t)m * K;
+  float lq[KT];
+  int32_t li[KT];
+#pragma unroll
+  for (int i = 0; i < KT; ++i) { lq[i] = -INFINITY; li[i] = 0x7FFFFFFF; }
+  float gk = -INFINITY;  // Gumbel-max: best perturbed log q of this lane
   int32_t gi = 0x7FFFFFFF;
   int gj = -1;
-  for (int j = tid; j < K; j += kSelThreads) {
-    const float qj = q[row + j];
-    const int32_t id = ids[row + j];
-    if (q_beats(qj, id, lq[tid][KT - 1], li[tid][KT - 1])) {
-      int pos = KT - 1;
-      while (pos > 0 && q_beats(qj, id, lq[tid][pos - 1], li[tid][pos - 1])) {
-        lq[tid][pos] = lq[tid][pos - 1];
-        li[tid][pos] = li[tid][pos - 1];
-        --pos;
-      }
-      lq[tid][pos] = qj;
-      li[tid][pos] = id;
+  constexpr int kBatch = 8;  // elements per lane loaded together (one latency per batch)
+  for (int j0 = 0; j0 < K; j0 += 32 * kBatch) {
+    float qb[kBatch], ub[kBatch];
+    int32_t ib[kBatch];
+#pragma unroll
+    for (int bb = 0; bb < kBatch; ++bb) {
+      const int j = j0 + bb * 32 + lane;
+      const bool in = j < K;
+      qb[bb] = in ? __ldg(q + row + j) : -INFINITY;
+      ib[bb] = in ? __ldg(ids + row + j) : 0x7FFFFFFF;
+      ub[bb] = (in && uniforms) ? __ldg(uniforms + row + j) : 0.5f;
     }
-    if (uniforms) {
-      const float s = qj > 0.f ? logf(qj) - logf(-logf(uniforms[row + j])) : -INFINITY;
-      if (gj < 0 || q_beats(s, id, gk, gi)) { gk = s; gi = id; gj = j; }
+#pragma unroll
+    for (int bb = 0; bb < kBatch; ++bb) {
+      const int j = j0 + bb * 32 + lane;
+      if (j >= K) break;
+      const float qj = qb[bb];
+      const int32_t id = ib[bb];
+      bool c[KT];
+#pragma unroll
+      for (int i = 0; i < KT; ++i) c[i] = q_beats(qj, id, lq[i], li[i]);
+#pragma unroll
+      for (int i = KT - 1; i > 0; --i) {
+        lq[i] = c[i] ? (c[i - 1] ? lq[i - 1] : qj) : lq[i];
+        li[i] = c[i] ? (c[i - 1] ? li[i - 1] : id) : li[i];
+      }
+      lq[0] = c[0] ? qj : lq[0];
+      li[0] = c[0] ? id : li[0];
+      if (uniforms) {
+        const float sj = qj > 0.f ? logf(qj) - logf(-logf(ub[bb])) : -INFINITY;
+        if (gj < 0 || q_beats(sj, id, gk, gi)) { gk = sj; gi = id; gj = j; }
+      }
     }
   }
-  // k_sel rounds: the best head over all threads' lists is the next output
-  int head = 0;
-  const float pv = parent_value ? parent_value[blockIdx.x] : 1.f;
+  const float pv = parent_value ? parent_value[m] : 1.f;
   for (int k = 0; k < k_sel; ++k) {
-    float key = head < KT ? lq[tid][head] : -INFINITY;
-    int32_t id = head < KT ? li[tid][head] : 0x7FFFFFFF;
-    int who = tid;
-    block_best(key, id, who, shk, shi, shw);
-    if (tid == who) ++head;
-    if (tid == 0) {
-      const size_t o = (size_t)blockIdx.x * k_sel + k;
+    float key = lq[0];
+    int32_t id = li[0];
+    int who = lane;
+    warp_best(key, id, who);
+    if (lane == who) {  // pop the head
+#pragma unroll
+      for (int i = 0; i + 1 < KT; ++i) { lq[i] = lq[i + 1]; li[i] = li[i + 1]; }
+      lq[KT - 1] = -INFINITY;
+      li[KT - 1] = 0x7FFFFFFF;
+    }
+    if (lane == 0) {
+      const size_t o = (size_t)m * k_sel + k;
       top_ids[o] = id;
       top_q[o] = key;
       if (top_value) top_value[o] = pv * key;
@@ -108,10 +124,10 @@ draft_select_kernel(const float* __restrict__ q, const int32_t* __restrict__ ids
   }
   if (uniforms) {
     int who = gj;  // carries the index of the winner's element
-    block_best(gk, gi, who, shk, shi, shw);
-    if (tid == 0) {
-      if (sample_id) sample_id[blockIdx.x] = gi;
-      if (sample_q) sample_q[blockIdx.x] = who >= 0 ? q[row + who] : 0.f;
+    warp_best(gk, gi, who);
+    if (lane == 0) {
+      if (sample_id) sample_id[m] = gi;
+      if (sample_q) sample_q[m] = who >= 0 ? q[row + who] : 0.f;
     }
   }
 }
@@ -119,6 +135,8 @@ draft_select_kernel(const float* __restrict__ q, const int32_t* __restrict__ ids
 // ---------------------------------------------------------------- K9
 constexpr int kVerThreads = 1024;
 constexpr int kVerCluster = 8;     // CTAs per chain (the vocabulary is split over them)
+constexpr int kMaxDrafts = 1024;   // drafts per chain (the entry point's bound)
+constexpr int kMaxCpw = 64;        // chunk sums kept per warp for the walk
 constexpr int kHashSlots = 8192;  // >= 2 x kSelectMaxK
 
 __device__ __forceinline__ uint32_t hash_slot(int32_t id) {
@@ -142,7 +160,7 @@ __device__ __forceinline__ uint32_t hash_slot(int32_t id) {
 // itself. Returns the token in the CTA that drew it and -1 in the others.
 __device__ int residual_draw(const float* __restrict__ prow, int64_t n, bool use_q,
                              const int32_t* tkey, const float* tval, float u, float* wtot,
-                             int* s_tok, float* cta_tot, int rank) {
+                             int* s_tok, float* cta_tot, float* csum, int rank) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int kWarps = kVerThreads / 32;
   const int64_t nch = (n + 31) / 32;
@@ -166,12 +184,19 @@ __device__ int residual_draw(const float* __restrict__ prow, int64_t n, bool use
     }
     return w > 0.f ? w : 0.f;
   };
+  // runs of at most kMaxCpw chunks keep their chunk sums in shared memory, so
+  // the walk reads the vocabulary again only in the crossing chunk
+  const bool keep = cpw <= kMaxCpw;
+  float* cs_w = csum + warp * kMaxCpw;
   for (int pass = 0; pass < 2; ++pass) {
     const bool sub = use_q && pass == 0;
-    float part = 0.f;  // this lane's share of the run (coalesced loads, no shuffles)
+    float run = 0.f;  // chunk sums added in chunk order (identical in every lane)
 #pragma unroll 8
-    for (int64_t c = c0; c < c1; ++c) part += weight(c * 32 + lane, sub);
-    const float run = warp_sum(part);  // identical in every lane
+    for (int64_t c = c0; c < c1; ++c) {
+      const float cs = warp_sum(weight(c * 32 + lane, sub));  // coalesced: one chunk per load
+      if (keep && lane == 0) cs_w[c - c0] = cs;
+      run += cs;
+    }
     if (lane == 0) wtot[warp] = run;
     if (threadIdx.x == 0) *s_tok = -1;
     cta_sync();
@@ -207,8 +232,12 @@ __device__ int residual_draw(const float* __restrict__ prow, int64_t n, bool use
         const int64_t c = b + lane;
         float cs = 0.f;
         if (c < c1) {
+          if (keep) {
+            cs = cs_w[c - c0];
+          } else {
 #pragma unroll 8
-          for (int i = 0; i < 32; ++i) cs += weight(c * 32 + i, sub);
+            for (int i = 0; i < 32; ++i) cs += weight(c * 32 + i, sub);
+          }
         }
         float sc = cs;  // inclusive scan of the chunk sums
 #pragma unroll
@@ -271,7 +300,10 @@ verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_
   float* tval = reinterpret_cast<float*>(vsm + kHashSlots);     // [kHashSlots]
   __shared__ float wtot[kVerThreads / 32];
   __shared__ float cta_tot;
-  __shared__ int s_hit, s_tok;
+  __shared__ float csum[(kVerThreads / 32) * kMaxCpw];
+  __shared__ int s_tok;
+  __shared__ int s_hit[kMaxDrafts];              // each draft's position in its candidates
+  __shared__ unsigned char s_state[kMaxDrafts];  // 0 not a candidate, 1 accepted, 2 rejected
   const int b = blockIdx.y;
   const int rank = (int)tc::cluster_ctarank();
   const float* pb = p + (size_t)b * (Kd + 1) * n;
@@ -282,30 +314,53 @@ verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_
   // after CTA 0's initialisation below)
   if (rank == 0)
     for (int i = threadIdx.x; i <= Kd; i += kVerThreads) ob[i] = -1;
-  for (int t = 0; t < Kd; ++t) {  // every CTA takes the same decisions
+  // every draft's accept test at once (each CTA of the cluster computes the
+  // same decisions): its position among its row's candidates, then
+  // r_t < p_t(x_t) / q_t(x_t) in fp32
+  for (int t = threadIdx.x; t < Kd; t += kVerThreads) s_hit[t] = K;
+  cta_sync();
+  const int64_t pairs = (int64_t)Kd * K;
+  for (int64_t e = threadIdx.x; e < pairs; e += kVerThreads) {
+    const int t = (int)(e / K);
+    const int j = (int)(e - (int64_t)t * K);
+    if (cand_ids[(size_t)b * Kd * K + e] == x[(size_t)b * Kd + t]) atomicMin(&s_hit[t], j);
+  }
+  cta_sync();
+  for (int t = threadIdx.x; t < Kd; t += kVerThreads) {
     const int32_t xt = x[(size_t)b * Kd + t];
+    const int hit = s_hit[t];
+    int st = 0;  // not a candidate of its row
+    if (hit < K && xt >= 0 && (int64_t)xt < n) {
+      const float px = pb[(size_t)t * n + xt];
+      const float qx = cand_q[((size_t)b * Kd + t) * K + hit];
+      st = r[(size_t)b * Kd + t] < px / qx ? 1 : 2;  // accepted : rejected
+    }
+    s_state[t] = (unsigned char)st;
+  }
+  cta_sync();
+  int stop = Kd;  // the first draft not accepted, in order
+  bool bad = false;
+  for (int t = 0; t < Kd; ++t) {
+    const int st = s_state[t];
+    if (st == 1) continue;
+    bad = st == 0;
+    stop = t;
+    break;
+  }
+  if (bad) {
+    if (rank == 0 && threadIdx.x == 0) {
+      record_error(err, kDevErrBadId);
+      out_count[b] = -1;
+    }
+    return;
+  }
+  if (rank == 0)
+    for (int t = threadIdx.x; t < stop; t += kVerThreads) ob[t] = x[(size_t)b * Kd + t];
+  if (stop < Kd) {
+    // rejected: the residual (p_t - q_t)+ over the vocabulary
+    const int t = stop;
     const int32_t* ci = cand_ids + ((size_t)b * Kd + t) * K;
     const float* cq = cand_q + ((size_t)b * Kd + t) * K;
-    if (threadIdx.x == 0) s_hit = K;
-    cta_sync();
-    for (int j = threadIdx.x; j < K; j += kVerThreads)
-      if (ci[j] == xt) atomicMin(&s_hit, j);
-    cta_sync();
-    const int hit = s_hit;
-    if (hit >= K || xt < 0 || (int64_t)xt >= n) {  // not a candidate of its row
-      if (rank == 0 && threadIdx.x == 0) {
-        record_error(err, kDevErrBadId);
-        out_count[b] = -1;
-      }
-      return;
-    }
-    const float px = pb[(size_t)t * n + xt];
-    const float qx = cq[hit];
-    if (r[(size_t)b * Kd + t] < px / qx) {
-      if (rank == 0 && threadIdx.x == 0) ob[t] = xt;
-      continue;
-    }
-    // rejected: the residual (p_t - q_t)+ over the vocabulary
     for (int i = threadIdx.x; i < kHashSlots; i += kVerThreads) tkey[i] = -1;
     cta_sync();
     for (int j = threadIdx.x; j < K; j += kVerThreads) {
@@ -323,7 +378,7 @@ verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_
     }
     cta_sync();
     const int tok = residual_draw(pb + (size_t)t * n, n, true, tkey, tval,
-                                  u[(size_t)b * (Kd + 1) + t], wtot, &s_tok, &cta_tot, rank);
+                                  u[(size_t)b * (Kd + 1) + t], wtot, &s_tok, &cta_tot, csum, rank);
     if (threadIdx.x == 0) {
       if (tok >= 0) ob[t] = tok;
       if (rank == 0) out_count[b] = t;
@@ -331,7 +386,7 @@ verify_chain_kernel(const float* __restrict__ p, int64_t n, int Kd, const int32_
     return;
   }
   const int tok = residual_draw(pb + (size_t)Kd * n, n, false, tkey, tval,
-                                u[(size_t)b * (Kd + 1) + Kd], wtot, &s_tok, &cta_tot, rank);
+                                u[(size_t)b * (Kd + 1) + Kd], wtot, &s_tok, &cta_tot, csum, rank);
   if (threadIdx.x == 0) {
     if (tok >= 0) ob[Kd] = tok;
     if (rank == 0) out_count[b] = Kd;
@@ -344,10 +399,11 @@ cudaError_t launch_draft_select(const float* q, const int32_t* ids, int M, int K
                                 const float* parent_value, const float* uniforms, int32_t* top_ids,
                                 float* top_q, float* top_value, int32_t* sample_id,
                                 float* sample_q, cudaStream_t s) {
+  const unsigned grid = (unsigned)((M + kSelThreads / 32 - 1) / (kSelThreads / 32));
 #define DS(KT)                                                                                  \
-  return launch_kernel(true, draft_select_kernel<KT>, dim3(M), dim3(kSelThreads), 0, s, q, ids, K, \
-                       k_sel, parent_value, uniforms, top_ids, top_q, top_value, sample_id,     \
-                       sample_q)
+  return launch_kernel(true, draft_select_kernel<KT>, dim3(grid), dim3(kSelThreads), 0, s, q, ids, \
+                       M, K, k_sel, parent_value, uniforms, top_ids, top_q, top_value,          \
+                       sample_id, sample_q)
   if (k_sel <= 1) DS(1);
   if (k_sel <= 2) DS(2);
   if (k_sel <= 4) DS(4);
