@@ -147,3 +147,17 @@ def test_verify_chain_bonus_only_and_bad_draft(L):
     assert host(count)[1] == -1
     assert L.last_device_error() == -7
     assert L.last_device_error() == 0
+
+
+@pytest.mark.parametrize("n", [40, 70, 300, 2049])
+def test_verify_chain_small_vocabularies(L, n):
+    """Vocabularies of a few 32-entry chunks: most CTAs of a chain's cluster
+    own an empty slice (n = 40 has two chunks for eight CTAs)."""
+    rng = np.random.default_rng(1000 + n)
+    B, Kd, K = 6, 2, 8
+    p, x, cid, cq, r, u = _chain_case(rng, B, Kd, K, n, equal_rows={1})
+    tokens, count = L.verify_chain(_t(p), _t(x), _t(cid), _t(cq), _t(r), _t(u))
+    tokens, count = host(tokens), host(count)
+    assert count[1] == Kd
+    assert _check_chain(p, x, cid, cq, r, u, tokens, count) <= 1
+    assert L.last_device_error() == 0
