@@ -40,8 +40,10 @@ struct Layout {
   int n_tickets = 0;  // ints at `tickets` zeroed by K1: row tickets then tile tickets
 };
 
-bool use_tc(int mode, int r, int T, int k_tile) {
-  return mode == LMHEAD_LOCAL && local_topk_tc_supported(r, T, k_tile);
+bool use_tc(int mode, int r, int T, int k_tile, int M) {
+  // small batches take the CUDA-core GEMV kernel where it applies
+  return mode == LMHEAD_LOCAL && local_topk_tc_supported(r, T, k_tile) &&
+         !local_topk_gemv_supported(M, r, T, k_tile);
 }
 
 bool needs_score_buffer(int mode, int k_tile) {
@@ -65,7 +67,7 @@ Layout layout_for(int mode, int64_t n, int d, int r, int M, int C_or_tile, int k
   L.u = off;
   off = round_up(off + (size_t)M * r * sizeof(bf16_t), 256);
   L.tickets = off;
-  const bool tc = use_tc(mode, r, C_or_tile, k_tile);
+  const bool tc = use_tc(mode, r, C_or_tile, k_tile, M);
   L.n_tickets = M + (tc ? local_topk_tc_tickets(n, M, C_or_tile) : 0);
   off = round_up(off + (size_t)L.n_tickets * sizeof(int), 256);
   if (tc) {
@@ -139,7 +141,7 @@ int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
   bf16_t* u = reinterpret_cast<bf16_t*>(ws + L.u);
   int* tickets = reinterpret_cast<int*>(ws + L.tickets);
   if (mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
-  const bool tc = use_tc(mode, r, C_or_tile, k_tile);
+  const bool tc = use_tc(mode, r, C_or_tile, k_tile, M);
   const bool zero = zero_tickets || tc;
   cudaError_t e = launch_project_u(B, h, d, r, M, u, zero ? tickets : nullptr,
                                    zero ? L.n_tickets : 0, s);

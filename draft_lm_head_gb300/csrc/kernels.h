@@ -23,6 +23,10 @@ cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int
                              int* zero_ptr, int zero_ints, cudaStream_t s);
 
 // K4 (CUDA cores): fused tile scores + per-tile top-k_tile, no score writeback.
+// For M <= kLocalGemvMaxM and tiles of 32..256 rows dividing 256 (k_tile <= 8,
+// r = 256) it runs the warp-per-row GEMV kernel.
+constexpr int kLocalGemvMaxM = 2;
+bool local_topk_gemv_supported(int M, int r, int T, int k_tile);
 cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
                                   int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,
                                   float* out_scores, cudaStream_t s);

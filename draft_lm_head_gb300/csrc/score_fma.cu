@@ -8,6 +8,7 @@
 // per row with the rank dimension split across lanes; u (M x r) sits in
 // shared memory as fp32. A CTA covers a block of up to kMB hidden vectors.
 #include <math.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -155,7 +156,179 @@ local_topk_fma_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u
   }
 }
 
+// ---------------------------------------------------------------- K4 (gemv)
+// One or two hidden vectors with tiles of 32-256 rows that divide 256: the
+// contraction is a GEMV (one or two FLOP per byte of A), so CUDA cores keep
+// pace with HBM and the tensor-core kernel's machinery (TMA ring, MMA issue,
+// TMEM) only adds latency. A warp scores eight rows at a time, each lane
+// reading one 16-byte piece of every row (r = 256: coalesced 512-byte
+// requests), the first eight rows issued before waiting for u (u comes from the projection kernel, A
+// does not); the lane's share of u sits in registers and a warp reduction
+// gives each row's score. The CTA's 256 rows hold 256 / T whole tiles; each
+// tile's top k_tile per hidden vector comes from one warp: every lane keeps a
+// sorted register list of its strided share of the tile's scores, then
+// k_tile rounds of a warp arg-best over the list heads (score descending,
+// then the smaller vocabulary id).
+constexpr int kGemvThreads = 256;
+
+
+__device__ __forceinline__ bool gemv_beats(float sa, int32_t ia, float sb, int32_t ib) {
+  return sa > sb || (sa == sb && ia < ib);
+}
+
+template <int MB, int KT>
+__global__ void __launch_bounds__(kGemvThreads, MB == 1 ? 4 : 3)  // measured best per MB
+local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u,
+                       const int32_t* __restrict__ token_ids, int64_t n, int r, int M, int T,
+                       int k_tile, int K, int32_t* __restrict__ out_ids,
+                       float* __restrict__ out_scores) {
+  __shared__ float sc[MB][kGemvThreads];
+  __shared__ int32_t svid[kGemvThreads];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row0 = (int64_t)blockIdx.x * kGemvThreads;
+  const int m0 = blockIdx.y * MB;
+  const int mb = min(MB, M - m0);
+  constexpr int kRows = 8;  // rows per batch and warp (loads in flight)
+  {
+    const int64_t pos = row0 + tid;
+    svid[tid] = pos < n ? (token_ids ? __ldg(token_ids + pos) : (int32_t)pos) : 0x7FFFFFFF;
+  }
+  // warp w scores rows w, w + 8, ... of the CTA's 256; lane L reads piece L
+  // of a row (r = 256: coalesced 512-byte requests)
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  uint4 a[kRows];
+  auto load_batch = [&](int bt) {
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      const int64_t pos = row0 + (int64_t)(bt * kRows + i) * 8 + warp;
+      const uint4* arow = reinterpret_cast<const uint4*>(A + (size_t)(pos < n ? pos : 0) * r);
+      a[i] = pos < n ? ldg_nc_v4(arow + lane) : zero;
+    }
+  };
+  load_batch(0);  // A before waiting for u
+  pdl_wait();     // u is written by the previous kernel
+  float uf[MB][8];
+#pragma unroll
+  for (int mm = 0; mm < MB; ++mm) {
+    uint4 uv = zero;
+    if (mm < mb) uv = *reinterpret_cast<const uint4*>(u + (size_t)(m0 + mm) * r + lane * 8);
+    unpack8(uv, uf[mm]);
+  }
+  constexpr int kBatches = kGemvThreads / 8 / kRows;  // 4 batches of 8 rows per warp
+  for (int bt = 0; bt < kBatches; ++bt) {
+    if (bt > 0) load_batch(bt);
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      float part[MB];
+      float f[8];
+      unpack8(a[i], f);
+#pragma unroll
+      for (int mm = 0; mm < MB; ++mm) {
+        part[mm] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part[mm] = fmaf(f[e], uf[mm][e], part[mm]);
+      }
+      const int rl = (bt * kRows + i) * 8 + warp;  // row within the CTA
+      const bool live = row0 + rl < n;
+#pragma unroll
+      for (int mm = 0; mm < MB; ++mm) {
+        const float sres = warp_sum(part[mm]);
+        if (lane == 0) sc[mm][rl] = live ? sres : -INFINITY;
+      }
+    }
+  }
+  cta_sync();
+  // one warp per (tile, hidden vector)
+  const int tpc = kGemvThreads / T;
+  const int jobs = tpc * mb;
+  for (int job = warp; job < jobs; job += kGemvThreads / 32) {
+    const int tl = job / mb, mm = job - tl * mb;
+    const int64_t tile = (int64_t)blockIdx.x * tpc + tl;
+    const int64_t t0 = tile * T;
+    if (t0 >= n) continue;
+    const int rows = (int)min((int64_t)T, n - t0);
+    float ls[KT];
+    int32_t lv[KT];
+#pragma unroll
+    for (int i = 0; i < KT; ++i) { ls[i] = -INFINITY; lv[i] = 0x7FFFFFFF; }
+    for (int j = lane; j < rows; j += 32) {
+      const float x = sc[mm][tl * T + j];
+      const int32_t id = svid[tl * T + j];
+      bool c[KT];
+#pragma unroll
+      for (int i = 0; i < KT; ++i) c[i] = gemv_beats(x, id, ls[i], lv[i]);
+#pragma unroll
+      for (int i = KT - 1; i > 0; --i) {
+        ls[i] = c[i] ? (c[i - 1] ? ls[i - 1] : x) : ls[i];
+        lv[i] = c[i] ? (c[i - 1] ? lv[i - 1] : id) : lv[i];
+      }
+      ls[0] = c[0] ? x : ls[0];
+      lv[0] = c[0] ? id : lv[0];
+    }
+    const int count = min(k_tile, rows);
+    const size_t base = (size_t)(m0 + mm) * K + (size_t)tile * k_tile;
+    for (int k = 0; k < count; ++k) {
+      float key = ls[0];
+      int32_t id = lv[0];
+      int who = lane;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ok = __shfl_xor_sync(0xFFFFFFFFu, key, off);
+        const int32_t oi = __shfl_xor_sync(0xFFFFFFFFu, id, off);
+        const int ow = __shfl_xor_sync(0xFFFFFFFFu, who, off);
+        if (gemv_beats(ok, oi, key, id)) { key = ok; id = oi; who = ow; }
+      }
+      if (lane == who) {  // pop the head
+#pragma unroll
+        for (int i = 0; i + 1 < KT; ++i) { ls[i] = ls[i + 1]; lv[i] = lv[i + 1]; }
+        ls[KT - 1] = -INFINITY;
+        lv[KT - 1] = 0x7FFFFFFF;
+      }
+      if (lane == 0) {
+        out_ids[base + k] = id;
+        if (out_scores) out_scores[base + k] = key;
+      }
+    }
+  }
+}
+
+template <int MB>
+cudaError_t launch_gemv_mb(const bf16_t* A, const bf16_t* u, const int32_t* token_ids, int64_t n,
+                           int r, int M, int T, int k_tile, int K, int32_t* out_ids,
+                           float* out_scores, cudaStream_t s) {
+  const size_t smem = 0;
+  dim3 grid((unsigned)((n + kGemvThreads - 1) / kGemvThreads), (unsigned)((M + MB - 1) / MB));
+#define GV(KT)                                                                                     \
+  {                                                                                                \
+    static int smem_set[64] = {0};                                                                 \
+    cudaError_t e = ensure_dynamic_smem(local_topk_gemv_kernel<MB, KT>, smem, smem_set);           \
+    if (e != cudaSuccess) return e;                                                                \
+    return launch_kernel(true, local_topk_gemv_kernel<MB, KT>, grid, dim3(kGemvThreads), smem, s, \
+                         A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores);            \
+  }
+  if (k_tile <= 1) GV(1)
+  if (k_tile <= 2) GV(2)
+  if (k_tile <= 4) GV(4)
+  GV(8)
+#undef GV
+}
+
+// LMHEAD_K4_GEMV = 0 keeps small batches off the GEMV kernel (measurements only).
+bool gemv_enabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("LMHEAD_K4_GEMV");
+    v = (e && e[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
+}
+
 }  // namespace
+
+bool local_topk_gemv_supported(int M, int r, int T, int k_tile) {
+  return gemv_enabled() && M <= kLocalGemvMaxM && r == 256 && T >= 32 &&
+         T <= kGemvThreads && kGemvThreads % T == 0 && k_tile <= 8;
+}
 
 cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
                                   int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,
@@ -163,6 +336,10 @@ cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_
   const int64_t tiles = (n + T - 1) / T;
   const int64_t full = n / T, tail = n - full * T;
   const int K = (int)(full * k_tile + (tail ? (tail < k_tile ? tail : k_tile) : 0));
+  if (local_topk_gemv_supported(M, r, T, k_tile)) {
+    if (M <= 1) return launch_gemv_mb<1>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s);
+    return launch_gemv_mb<2>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s);
+  }
   const size_t smem = (size_t)kMB * r * sizeof(float);
   if (smem > 48 * 1024) {
     static int smem_set[64] = {0};
