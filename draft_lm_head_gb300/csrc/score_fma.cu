@@ -176,8 +176,10 @@ __device__ __forceinline__ bool gemv_beats(float sa, int32_t ia, float sb, int32
   return sa > sb || (sa == sb && ia < ib);
 }
 
-template <int MB, int KT>
-__global__ void __launch_bounds__(kGemvThreads, MB == 1 ? 4 : 3)  // measured best per MB
+// DB: the next batch of rows is requested before the current one is used
+// (more registers, so fewer CTAs per SM).
+template <int MB, int KT, bool DB>
+__global__ void __launch_bounds__(kGemvThreads, DB ? (MB == 1 ? 3 : 2) : (MB == 1 ? 4 : 3))
 local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u,
                        const int32_t* __restrict__ token_ids, int64_t n, int r, int M, int T,
                        int k_tile, int K, int32_t* __restrict__ out_ids,
@@ -216,12 +218,20 @@ local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ 
   }
   constexpr int kBatches = kGemvThreads / 8 / kRows;  // 4 batches of 8 rows per warp
   for (int bt = 0; bt < kBatches; ++bt) {
-    if (bt > 0) load_batch(bt);
+    uint4 cur[kRows];  // this batch; with DB the next one is requested before it is used
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) cur[i] = a[i];
+    if (DB && bt + 1 < kBatches) load_batch(bt + 1);
+    if (!DB && bt > 0) {
+      load_batch(bt);
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) cur[i] = a[i];
+    }
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {
       float part[MB];
       float f[8];
-      unpack8(a[i], f);
+      unpack8(cur[i], f);
 #pragma unroll
       for (int mm = 0; mm < MB; ++mm) {
         part[mm] = 0.f;
@@ -292,7 +302,7 @@ local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ 
   }
 }
 
-template <int MB>
+template <int MB, bool DB>
 cudaError_t launch_gemv_mb(const bf16_t* A, const bf16_t* u, const int32_t* token_ids, int64_t n,
                            int r, int M, int T, int k_tile, int K, int32_t* out_ids,
                            float* out_scores, cudaStream_t s) {
@@ -301,9 +311,9 @@ cudaError_t launch_gemv_mb(const bf16_t* A, const bf16_t* u, const int32_t* toke
 #define GV(KT)                                                                                     \
   {                                                                                                \
     static int smem_set[64] = {0};                                                                 \
-    cudaError_t e = ensure_dynamic_smem(local_topk_gemv_kernel<MB, KT>, smem, smem_set);           \
+    cudaError_t e = ensure_dynamic_smem(local_topk_gemv_kernel<MB, KT, DB>, smem, smem_set);           \
     if (e != cudaSuccess) return e;                                                                \
-    return launch_kernel(true, local_topk_gemv_kernel<MB, KT>, grid, dim3(kGemvThreads), smem, s, \
+    return launch_kernel(true, local_topk_gemv_kernel<MB, KT, DB>, grid, dim3(kGemvThreads), smem, s, \
                          A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores);            \
   }
   if (k_tile <= 1) GV(1)
@@ -337,8 +347,11 @@ cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_
   const int64_t full = n / T, tail = n - full * T;
   const int K = (int)(full * k_tile + (tail ? (tail < k_tile ? tail : k_tile) : 0));
   if (local_topk_gemv_supported(M, r, T, k_tile)) {
-    if (M <= 1) return launch_gemv_mb<1>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s);
-    return launch_gemv_mb<2>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s);
+    // measured: one hidden vector, four CTAs per SM (all 501 CTAs of the
+    // 128256-row head resident at once); two, the next rows requested early
+    if (M <= 1)
+      return launch_gemv_mb<1, false>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s);
+    return launch_gemv_mb<2, true>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s);
   }
   const size_t smem = (size_t)kMB * r * sizeof(float);
   if (smem > 48 * 1024) {
