@@ -259,6 +259,21 @@ def test_local_long_tiles(L, M, n, T, k):
     P.check_order("local", host(ids), host(sc), T, k, n)
 
 
+# More 256-row tiles than SMs (n = 50000 is 196 tiles, the last one ragged):
+# tiles claimed dynamically past the first round, 256-row MMAs, one and two
+# 128-lane blocks of hidden vectors.
+@pytest.mark.parametrize("M", [3, 64, 150])
+@pytest.mark.parametrize("k", [1, 2, 8])
+def test_local_more_tiles_than_sms(L, M, k):
+    case = make_case(50000, 64, 16, M, seed=23, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    ids, sc = L.lowrank_score_topk(L.LOCAL, A, B, h, tok, 256, k, with_scores=True)
+    assert L.last_device_error() == 0
+    _, S, _, SL = oracle_scores(case, with_slack=True)
+    P.check_ids("local", host(ids), S, case["tok"], 256, k, slack_pos=SL)
+    P.check_order("local", host(ids), host(sc), 256, k, 50000)
+
+
 @pytest.mark.parametrize("M", [1, 17, 300])
 def test_dense_head_blocks(L, M):
     # CUDA cores at M = 1; tensor cores above, M > 256 in blocks of 256 hidden
