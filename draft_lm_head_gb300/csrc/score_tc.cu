@@ -18,7 +18,12 @@
 //    of (score, position) in registers. A tile boundary flushes the list:
 //    ids are written through token_ids (ties: smaller vocabulary id).
 //  - Tiles of a multiple of 128 rows (the usual case) are scheduled
-//    dynamically, whole tiles per CTA (local_topk_tc_dyn_kernel). Otherwise
+//    dynamically, whole tiles per CTA (local_topk_tc_dyn_kernel). For tiles
+//    of a multiple of 256 rows it uses 256-row chunks: 256-row boxes and
+//    N = 256 MMAs into two TMEM accumulators. One tcgen05.mma (M = 128,
+//    K = 16) occupies the tensor pipe about the same time at N = 128 as at
+//    N = 256 (measured), so the wider MMA halves the tensor time per byte
+//    of A. Otherwise
 //    CTAs take balanced contiguous chunk ranges; a tile cut by a CTA boundary
 //    leaves partial lists in the workspace and the last CTA to finish a part
 //    (atomic ticket, no waiting) merges them.
@@ -529,8 +534,8 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
 }
 
 // ---------------------------------------------------------------- dynamic tiles
-// Variant for tiles of a multiple of 128 rows: whole tiles are the unit of
-// work. CTA b first takes tile b (so it can stream A before the projection
+// Variant for tiles of a multiple of 128 rows (chunks of CH = 128 or 256
+// rows): whole tiles are the unit of work. CTA b first takes tile b (so it can stream A before the projection
 // kernel finishes), then claims tiles G, G+1, ... from a counter in the
 // workspace (zeroed by the projection kernel), so SMs that get their data
 // faster take more tiles. Chunk descriptors reach the MMA and epilogue
