@@ -65,3 +65,12 @@ def test_reference_arm_other_ranks_do_nothing(monkeypatch, capsys):
 
     assert bench.run_reference(Args()) is None
     assert capsys.readouterr().out == ""
+
+
+def test_workload_config_names_the_headline_workload():
+    # both arms print this dict; the candidate count is the local head's
+    c = bench.workload_config(64, 2, 4)
+    assert (c["n"], c["d"], c["r"], c["M"], c["tile"], c["k_tile"]) == (128256, 4096, 256, 64, 256, 2)
+    assert c["candidates"] == 1002 == (128256 // 256) * 2
+    assert c["parallelism"] == "replicas x2 (independent hidden vectors)"
+    assert "> 2x L2" in c["l2"] and "> 2x L2" not in bench.workload_config(64, 1, 1)["l2"]
