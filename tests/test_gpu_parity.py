@@ -274,6 +274,27 @@ def test_local_more_tiles_than_sms(L, M, k):
     P.check_order("local", host(ids), host(sc), 256, k, 50000)
 
 
+# One or two hidden vectors at r = 256 take the warp-per-row GEMV scoring
+# kernel: every tile size it serves (32-256 rows), k_tile 1 to 8 (3 is not a
+# power of two), a ragged last CTA block and a ragged last tile.
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("T,k", [(32, 1), (64, 3), (128, 4), (256, 2), (256, 8)])
+def test_local_gemv_small_batches(L, M, T, k):
+    case = make_case(5037, 512, 256, M, seed=29, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    ids, sc = L.lowrank_score_topk(L.LOCAL, A, B, h, tok, T, k, with_scores=True)
+    assert L.last_device_error() == 0
+    _, S, _, SL = oracle_scores(case, with_slack=True)
+    P.check_ids("local", host(ids), S, case["tok"], T, k, slack_pos=SL)
+    P.check_order("local", host(ids), host(sc), T, k, 5037)
+    assert ids.shape[1] == O.local_candidate_count(5037, T, k)
+    lg_ids, lg, q = L.two_stage(L.LOCAL, W, A, B, h, tok, T, k)
+    h64 = O.bf16_bits_to_f64(case["h"])
+    ex = P.exact_logits(case["W"], h64, host(lg_ids))
+    P.check_logits(host(lg), ex)
+    P.check_q(host(q), ex)
+
+
 @pytest.mark.parametrize("M", [1, 17, 300])
 def test_dense_head_blocks(L, M):
     # CUDA cores at M = 1; tensor cores above, M > 256 in blocks of 256 hidden
