@@ -162,15 +162,14 @@ local_topk_fma_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u
 // pace with HBM and the tensor-core kernel's machinery (TMA ring, MMA issue,
 // TMEM) only adds latency. A warp scores eight rows at a time, each lane
 // reading one 16-byte piece of every row (r = 256: coalesced 512-byte
-// requests), the first eight rows issued before waiting for u (u comes from the projection kernel, A
-// does not); the lane's share of u sits in registers and a warp reduction
-// gives each row's score. The CTA's 256 rows hold 256 / T whole tiles; each
+// requests), the first eight rows requested before waiting for u (u comes
+// from the projection kernel, A does not); the lane's share of u sits in
+// registers and a warp reduction gives each row's score. The CTA's 256 rows hold 256 / T whole tiles; each
 // tile's top k_tile per hidden vector comes from one warp: every lane keeps a
 // sorted register list of its strided share of the tile's scores, then
 // k_tile rounds of a warp arg-best over the list heads (score descending,
 // then the smaller vocabulary id).
 constexpr int kGemvThreads = 256;
-
 
 __device__ __forceinline__ bool gemv_beats(float sa, int32_t ia, float sb, int32_t ib) {
   return sa > sb || (sa == sb && ia < ib);
@@ -218,15 +217,11 @@ local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ 
   }
   constexpr int kBatches = kGemvThreads / 8 / kRows;  // 4 batches of 8 rows per warp
   for (int bt = 0; bt < kBatches; ++bt) {
+    if (!DB && bt > 0) load_batch(bt);
     uint4 cur[kRows];  // this batch; with DB the next one is requested before it is used
 #pragma unroll
     for (int i = 0; i < kRows; ++i) cur[i] = a[i];
     if (DB && bt + 1 < kBatches) load_batch(bt + 1);
-    if (!DB && bt > 0) {
-      load_batch(bt);
-#pragma unroll
-      for (int i = 0; i < kRows; ++i) cur[i] = a[i];
-    }
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {
       float part[MB];
@@ -306,20 +301,14 @@ template <int MB, bool DB>
 cudaError_t launch_gemv_mb(const bf16_t* A, const bf16_t* u, const int32_t* token_ids, int64_t n,
                            int r, int M, int T, int k_tile, int K, int32_t* out_ids,
                            float* out_scores, cudaStream_t s) {
-  const size_t smem = 0;
   dim3 grid((unsigned)((n + kGemvThreads - 1) / kGemvThreads), (unsigned)((M + MB - 1) / MB));
-#define GV(KT)                                                                                     \
-  {                                                                                                \
-    static int smem_set[64] = {0};                                                                 \
-    cudaError_t e = ensure_dynamic_smem(local_topk_gemv_kernel<MB, KT, DB>, smem, smem_set);           \
-    if (e != cudaSuccess) return e;                                                                \
-    return launch_kernel(true, local_topk_gemv_kernel<MB, KT, DB>, grid, dim3(kGemvThreads), smem, s, \
-                         A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores);            \
-  }
-  if (k_tile <= 1) GV(1)
-  if (k_tile <= 2) GV(2)
-  if (k_tile <= 4) GV(4)
-  GV(8)
+#define GV(KT)                                                                                \
+  return launch_kernel(true, local_topk_gemv_kernel<MB, KT, DB>, grid, dim3(kGemvThreads), 0, s, \
+                       A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores);
+  if (k_tile <= 1) GV(1);
+  if (k_tile <= 2) GV(2);
+  if (k_tile <= 4) GV(4);
+  GV(8);
 #undef GV
 }
 
