@@ -150,3 +150,49 @@ def test_cluster_entry_points_validate_before_launch(lib):
     assert call(W=_p(ok + 8)) == -3
     assert call(ws=None) == -4
     assert call(wsb=16) == -4
+
+
+def _declarations():
+    """name -> (return type text, [parameter type texts]) from include/*.h."""
+    out = {}
+    for hdr in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(hdr).read(), flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"([\w\s\*]+?)\b(lmhead_\w+)\s*\(([^;]*?)\)\s*;", text):
+            ret, name, params = m.group(1).strip(), m.group(2), m.group(3).strip()
+            plist = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
+            out[name] = (ret.split()[-1] if ret else "", plist)
+    return out
+
+
+def _ctype_of(decl: str):
+    c = ctypes
+    if "*" in decl or decl.startswith("lmhead_stream"):
+        return c.c_void_p
+    if decl.startswith("int64_t"):
+        return c.c_int64
+    if decl.startswith("size_t"):
+        return c.c_size_t
+    if decl.startswith("float"):
+        return c.c_float
+    if decl.split()[0] in ("int", "int32_t"):
+        return c.c_int
+    raise AssertionError(f"unclassified parameter type: {decl}")
+
+
+def test_binding_argument_types_match_the_header():
+    """Every ctypes signature in the binding passes exactly the header's
+    parameters, in order and by ABI class (pointer, int, int64, size_t,
+    float): a mismatch would hand the library shifted arguments."""
+    from draft_lm_head_gb300 import _lib
+    decls = _declarations()
+    assert set(decls) == set(_lib.SIGNATURES)
+    for name, (ret, params) in decls.items():
+        restype, argtypes = _lib.SIGNATURES[name]
+        want = [_ctype_of(p) for p in params]
+        assert list(argtypes) == want, name
+        if ret.endswith("*") or ret == "char*":
+            assert restype in (ctypes.c_char_p, ctypes.c_void_p), name
+        else:
+            assert restype == {"int": ctypes.c_int, "int64_t": ctypes.c_int64,
+                               "size_t": ctypes.c_size_t}[ret], name
