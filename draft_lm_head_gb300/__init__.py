@@ -54,6 +54,19 @@ def _typed(t: Optional[torch.Tensor], dtype, name: str) -> int:
     return t.data_ptr()
 
 
+def _check_shapes(device, **named) -> None:
+    """Host-side size checks before any pointer reaches the library: the C ABI
+    takes sizes from the caller, so a tensor of the wrong shape would make a
+    kernel read or write outside it. named: name -> (tensor or None, shape)."""
+    for name, (t, want) in named.items():
+        if t is None:
+            continue
+        if tuple(t.shape) != tuple(want):
+            raise ValueError(f"{name}: expected shape {tuple(want)}, got {tuple(t.shape)}")
+        if device is not None and t.device != device:
+            raise ValueError(f"{name}: on {t.device}, expected {device}")
+
+
 def version() -> int:
     return load().lmhead_version()
 
@@ -97,6 +110,7 @@ def project_u(B: torch.Tensor, h: torch.Tensor, out: Optional[torch.Tensor] = No
               stream=None) -> torch.Tensor:
     r, d = B.shape
     M = h.shape[0]
+    _check_shapes(B.device, h=(h, (M, d)), out=(out, (M, r)))
     u = out if out is not None else torch.empty((M, r), dtype=torch.bfloat16, device=h.device)
     check(load().lmhead_project_u(_bf16(B, "B"), _bf16(h, "h"), d, r, M, _bf16(u, "u"),
                                   _stream_ptr(stream)), "project_u")
@@ -109,6 +123,7 @@ def lowrank_score_topk(mode: int, A: torch.Tensor, B: torch.Tensor, h: torch.Ten
     n, r = A.shape
     d = B.shape[1]
     M = h.shape[0]
+    _check_shapes(A.device, B=(B, (r, d)), h=(h, (M, d)), token_ids=(token_ids, (n,)))
     K = candidate_count(mode, n, C_or_tile, k_tile)
     ids = torch.empty((M, K), dtype=torch.int32, device=h.device)
     scores = torch.empty((M, K), dtype=torch.float32, device=h.device) if with_scores else None
@@ -125,6 +140,7 @@ def gather_logits(W: torch.Tensor, h: torch.Tensor, ids: torch.Tensor,
                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     n, d = W.shape
     M, K = ids.shape
+    _check_shapes(W.device, h=(h, (M, d)), ids=(ids, (M, K)), out=(out, (M, K)))
     L = out if out is not None else torch.empty((M, K), dtype=torch.float32, device=h.device)
     check(load().lmhead_gather_logits(_bf16(W, "W"), _bf16(h, "h"), _typed(ids, torch.int32, "ids"),
                                       n, d, M, K, _typed(L, torch.float32, "out"),
@@ -135,6 +151,7 @@ def gather_logits(W: torch.Tensor, h: torch.Tensor, ids: torch.Tensor,
 def candidate_softmax(logits: torch.Tensor, temperature: float = 1.0,
                       out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     M, K = logits.shape
+    _check_shapes(logits.device, out=(out, (M, K)))
     q = out if out is not None else torch.empty_like(logits)
     check(load().lmhead_candidate_softmax(_typed(logits, torch.float32, "logits"), M, K,
                                           float(temperature), _typed(q, torch.float32, "out"),
@@ -156,6 +173,9 @@ def two_stage(mode: int, W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, h: t
         q = torch.empty((M, K), dtype=torch.float32, device=h.device)
     else:
         ids, L, q = out
+    _check_shapes(W.device, A=(A, (n, r)), B=(B, (r, d)), h=(h, (M, d)),
+                  token_ids=(token_ids, (n,)), ids=(ids, (M, K)), logits=(L, (M, K)),
+                  q=(q, (M, K)))
     nbytes = workspace_size(mode, n, d, r, M, C_or_tile, k_tile)
     ws = _ws(workspace, nbytes, h.device)
     check(load().lmhead_two_stage(
@@ -176,6 +196,7 @@ def dense_head(W: torch.Tensor, h: torch.Tensor, temperature: float = 1.0, with_
         q = torch.empty((M, n), dtype=torch.float32, device=h.device) if with_q else None
     else:
         L, q = out
+    _check_shapes(W.device, h=(h, (M, d)), logits=(L, (M, n)), q=(q, (M, n)))
     check(load().lmhead_dense_head(_bf16(W, "W"), _bf16(h, "h"), n, d, M, float(temperature),
                                    _typed(L, torch.float32, "logits"), _typed(q, torch.float32, "q"),
                                    _stream_ptr(stream)), "dense_head")
@@ -191,6 +212,7 @@ def pruned_head(W_pruned: torch.Tensor, h: torch.Tensor, temperature: float = 1.
         q = torch.empty((M, n_keep), dtype=torch.float32, device=h.device) if with_q else None
     else:
         L, q = out
+    _check_shapes(W_pruned.device, h=(h, (M, d)), logits=(L, (M, n_keep)), q=(q, (M, n_keep)))
     check(load().lmhead_pruned_head(_bf16(W_pruned, "W_pruned"), _bf16(h, "h"), n_keep, d, M,
                                     float(temperature), _typed(L, torch.float32, "logits"),
                                     _typed(q, torch.float32, "q"), _stream_ptr(stream)),
@@ -233,6 +255,8 @@ def cluster_two_stage(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, h: torc
         q = torch.empty((M, K), dtype=torch.float32, device=dev)
     else:
         groups, ids, L, q = out
+    _check_shapes(W.device, A=(A, (n, r)), B=(B, (r, d)), h=(h, (M, d)), groups=(groups, (M, G)),
+                  ids=(ids, (M, K)), logits=(L, (M, K)), q=(q, (M, K)))
     gs = torch.empty((M, G), dtype=torch.float32, device=dev) if with_group_scores else None
     nbytes = cluster_workspace_size(n, d, r, M, group, G)
     ws = _ws(workspace, nbytes, dev)
@@ -254,6 +278,8 @@ def draft_select(q: torch.Tensor, ids: torch.Tensor, k_sel: int,
     without uniforms."""
     M, K = q.shape
     dev = q.device
+    _check_shapes(dev, ids=(ids, (M, K)), parent_value=(parent_value, (M,)),
+                  uniforms=(uniforms, (M, K)))
     top_ids = torch.empty((M, k_sel), dtype=torch.int32, device=dev)
     top_q = torch.empty((M, k_sel), dtype=torch.float32, device=dev)
     top_value = torch.empty((M, k_sel), dtype=torch.float32, device=dev)
@@ -277,6 +303,8 @@ def verify_chain(p: torch.Tensor, x: torch.Tensor, cand_ids: torch.Tensor, cand_
     Kd = Kd1 - 1
     K = cand_ids.shape[-1]
     dev = p.device
+    _check_shapes(dev, x=(x, (B, Kd)), cand_ids=(cand_ids, (B, Kd, K)),
+                  cand_q=(cand_q, (B, Kd, K)), r=(r, (B, Kd)), u=(u, (B, Kd + 1)))
     tokens = torch.empty((B, Kd + 1), dtype=torch.int32, device=dev)
     count = torch.empty(B, dtype=torch.int32, device=dev)
     check(load().lmhead_verify_chain(
