@@ -300,7 +300,8 @@ int lmhead_draft_select(const float* q, const int32_t* ids, int M, int K, int k_
  *             or bonus token, then -1; out_count  B int32: drafts accepted
  *             (0..Kd), or -1 when a drafted token is not a candidate (also
  *             recorded as LMHEAD_ERR_DEVICE_CHECK, see lmhead_last_device_error).
- * One CTA per chain; Kd may be 0 (bonus draw only).
+ * One 8-CTA thread-block cluster per chain (the vocabulary split over its CTAs); Kd may be
+ * 0 (bonus draw only).
  */
 int lmhead_verify_chain(const float* p, int64_t n, int B, int Kd, const int32_t* x,
                         const int32_t* cand_ids, const float* cand_q, int K, const float* r,
