@@ -8,8 +8,9 @@ Workloads (seeded, synthetic; see synth/):
      global C=1002 and 1024 for the recall comparison
   3  n=201088 d=2880 r=256, M=80 (8 sequences x 10-node tree): local 256/2; global C=1024
   4  n=151936 d=5120 r=512, M in {1,8,32,128,512}: local 256/4; dense; pruned 32000
-Recall of the exact full-head Top-{1,8,64} is written to gpurun_out/recall_*.json
-when that folder exists (a report, not a pass/fail criterion).
+Recall of the exact full-head Top-{1,8,64} is printed, and written to
+$LMHEAD_REPORT_DIR/recall_*.json when that variable names a folder (a report,
+not a pass/fail criterion).
 """
 import json
 import os
@@ -25,7 +26,7 @@ import parity as P
 
 pytestmark = pytest.mark.gpu
 
-OUT = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
+OUT = os.environ.get("LMHEAD_REPORT_DIR", "")
 
 
 @pytest.fixture(scope="module")
