@@ -12,7 +12,7 @@ route lost acceptance length against the full head, which is why the notes
 chose the token-level route; it is built here as a second candidate scheme on
 the same library.
 
-Readings where the section is silent (also listed in the design notes):
+Readings where the section is silent (numbered R21-R23):
   R21 A group is `group` consecutive rows of the head as stored (rows
       [g*group, (g+1)*group)), so a selected group is one contiguous block of
       W. The group size must divide n (every vocabulary size in the workloads

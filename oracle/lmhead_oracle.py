@@ -25,7 +25,7 @@ NumPy float64, on the same bf16 input bits that the GPU consumes. Sources:
   (ai-engineering.com.cn): the draft distribution q is what the accept/reject
   rule consumes. Together these are why stage 2 ends in a softmax.
 
-Readings where the pages are silent (each also listed in the design notes):
+Readings where the pages are silent (numbered R3-R15):
   R3  u is rounded to bf16 after the projection (the pseudocode's u = B @ h on
       bf16 tensors); the rounding is decided in fp32, as the kernel decides it.
   R4  scores are never rounded below fp32 (fp64 here).

@@ -16,7 +16,7 @@ Sources:
   the target. The page's exercise checks the output distribution against
   plain sampling from the target (total variation < 0.01 over 10K samples).
 
-Readings (also listed in the design notes):
+Readings (numbered R17-R20):
   R17 The page's printed listing subtracts the scalar q(x_t) from the target
       row; the exactness the page states (the output is distributed as p)
       holds for the pointwise residual (p - q)+ with the whole draft

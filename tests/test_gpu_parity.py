@@ -297,8 +297,8 @@ def test_local_gemv_small_batches(L, M, T, k):
 
 @pytest.mark.parametrize("M", [1, 17, 300])
 def test_dense_head_blocks(L, M):
-    # CUDA cores at M = 1; tensor cores above, M > 256 in blocks of 256 hidden
-    # vectors; n not a multiple of 128
+    # tensor cores at every M (N = M hidden vectors per MMA, M > 256 in blocks
+    # of 256); n not a multiple of 128
     case = make_case(1000, 96, 16, M, seed=18, plain_h=True)
     W, A, B, h, tok = _dev(case)
     lg, q = L.dense_head(W, h)
