@@ -79,9 +79,11 @@ def workload_case(wl, M, shuffle=None, tree=None, stream_offset=0):
             "h": h, "t": t, "counts": head["counts"], "n": wl.n, "d": wl.d, "r": wl.r, "M": M}
 
 
-def oracle_scores(case, with_slack=False):
+def oracle_scores(case, with_slack=False, M_call=None):
     """Oracle u (bf16 grid, fp64) and position-ordered scores M x n (and the
-    u-rounding slack of tests/parity.py when asked)."""
+    u-rounding slack of tests/parity.py when asked). M_call: hidden vectors
+    of the library call that produced the GPU side (it picks the projection
+    kernel, hence the slack); default the rows of case["h"]."""
     import parity
     A64 = O.bf16_bits_to_f64(case["A"])
     B64 = O.bf16_bits_to_f64(case["B"])
@@ -89,5 +91,5 @@ def oracle_scores(case, with_slack=False):
     u = O.project_u(B64, h64)
     S = O.lowrank_scores(A64, u)
     if with_slack:
-        return u, S, h64, parity.u_slack(A64, B64, h64)
+        return u, S, h64, parity.u_slack(A64, B64, h64, M_call)
     return u, S, h64

@@ -31,7 +31,7 @@ def _check(case, group, G, groups, ids, lg, q, gs, temperature=1.0, rows=None):
     rows = np.arange(case["M"]) if rows is None else np.asarray(rows)
     sub = dict(case)
     sub["h"] = case["h"][rows]
-    u, S, h64, SL = oracle_scores(sub, with_slack=True)
+    u, S, h64, SL = oracle_scores(sub, with_slack=True, M_call=case["M"])
     groups, ids, lg, q, gs = groups[rows], ids[rows], lg[rows], q[rows], gs[rows]
     excused = P.check_groups(groups, S, group, G, slack_pos=SL)
     M = len(rows)

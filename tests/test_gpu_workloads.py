@@ -34,25 +34,58 @@ def L():
     return lib()
 
 
-def _run(L, case, mode, C, k, rows=None):
+def _run(L, case, mode, C, k, temperature=1.0):
     W, A, B = dev_bf16(case["W"]), dev_bf16(case["A"]), dev_bf16(case["B"])
     h, tok = dev_bf16(case["h"]), dev_i32(case["tok"])
     md = L.LOCAL if mode == "local" else L.GLOBAL
-    ids, lg, q = L.two_stage(md, W, A, B, h, tok, C, k)
+    ids, lg, q = L.two_stage(md, W, A, B, h, tok, C, k, temperature=temperature)
     assert L.last_device_error() == 0
     return host(ids), host(lg), host(q)
 
 
-def _check(case, mode, C, k, ids, lg, q, rows=None):
+def _gpu_u(L, case):
+    """u as the library's projection computes it for this call's (d, M)
+    (the kernel is chosen by d and M only, and sums in a fixed order)."""
+    import torch
+    u = L.project_u(dev_bf16(case["B"]), dev_bf16(case["h"]))
+    return host(u.view(torch.int16)).view(np.uint16)
+
+
+def _check(L, case, mode, C, k, ids, lg, q, rows=None, temperature=1.0, name=None):
+    """Parity of one call on the rows `rows` (default all), recorded in the
+    session's parity report: excused ids split into the 1e-3 band and the
+    u-rounding slack, u elements that rounded the other way, and the spread
+    of q (so a one-hot q, where the 1e-4 check is vacuous, shows)."""
     rows = np.arange(case["M"]) if rows is None else np.asarray(rows)
     sub = dict(case)
     sub["h"] = case["h"][rows]
-    _, S, h64, SL = oracle_scores(sub, with_slack=True)
-    excused = P.check_ids(mode, ids[rows], S, case["tok"], C, k, slack_pos=SL)
+    _, S, h64, SL = oracle_scores(sub, with_slack=True, M_call=case["M"])
+    counts = P.check_ids(mode, ids[rows], S, case["tok"], C, k, slack_pos=SL)
     ex = P.exact_logits(case["W"], h64, ids[rows])
     floor = P.check_logits(lg[rows], ex)
-    P.check_q(q[rows], ex)
-    return excused, floor
+    bite = P.check_q(q[rows], ex, temperature)
+    flips, amb = P.check_u(_gpu_u(L, case)[rows], O.bf16_bits_to_f64(case["B"]), h64,
+                           M_call=case["M"])
+    label = name or f"{mode} n={case['n']} M={case['M']}"
+    P.record(label, mode=mode, M=int(case["M"]), rows=int(len(rows)), **counts,
+             logit_floor=floor, **bite, u_flips=flips, u_ambiguous=amb,
+             temperature=float(temperature))
+    return counts
+
+
+def _candidate_temperature(case, mode, C, k):
+    """The temperature at which q bites: the standard deviation of the exact
+    logits over the oracle's own candidates of row 0 (oracle only)."""
+    A64 = O.bf16_bits_to_f64(case["A"])
+    h0 = O.bf16_bits_to_f64(case["h"][:1])
+    u = O.project_u(O.bf16_bits_to_f64(case["B"]), h0)
+    S = O.lowrank_scores(A64, u)[0]
+    if mode == "local":
+        ids, _ = O.local_topk(S, case["tok"], C, k)
+    else:
+        ids, _ = O.global_topk(S, case["tok"], C)
+    Lx = O.candidate_logits(O.bf16_bits_to_f64(case["W"][ids]), h0[0], np.arange(len(ids)))
+    return float(np.std(Lx))
 
 
 def _dense_exact(W_bits, h64, block=16384):
@@ -75,10 +108,11 @@ def test_workload0_tiny(L):
         case = workload_case(wl, 1, shuffle=shuffle)
         ids, lg, q = _run(L, case, "local", wl.T, wl.k_tile)
         assert ids.shape == (1, 128)
-        _check(case, "local", wl.T, wl.k_tile, ids, lg, q)
+        _check(L, case, "local", wl.T, wl.k_tile, ids, lg, q,
+               name=f"wl0 local 128/4 {'shuffled' if shuffle else 'identity'} M=1")
     case = workload_case(wl, 1)
     ids, lg, q = _run(L, case, "global", wl.C, 0)
-    _check(case, "global", wl.C, 0, ids, lg, q)
+    _check(L, case, "global", wl.C, 0, ids, lg, q, name="wl0 global C=128 M=1")
 
 
 @pytest.mark.parametrize("M", [1, 4, 8])
@@ -87,7 +121,7 @@ def test_workload1_global(L, M):
     case = workload_case(wl, M)
     ids, lg, q = _run(L, case, "global", wl.C, 0)
     assert ids.shape == (M, 1024)
-    _check(case, "global", wl.C, 0, ids, lg, q)
+    _check(L, case, "global", wl.C, 0, ids, lg, q, name=f"wl1 global C=1024 M={M}")
 
 
 @pytest.mark.parametrize("M", [1, 8, 16, 32, 64])
@@ -96,12 +130,16 @@ def test_workload2_local(L, M):
     case = workload_case(wl, M)
     ids, lg, q = _run(L, case, "local", wl.T, wl.k_tile)
     assert ids.shape == (M, 1002)
-    _check(case, "local", wl.T, wl.k_tile, ids, lg, q)
+    _check(L, case, "local", wl.T, wl.k_tile, ids, lg, q, name=f"wl2 local 256/2 M={M}")
     if M == 64:
         h64 = O.bf16_bits_to_f64(case["h"])
         Z = _dense_exact(case["W"], h64)
-        g1002, _, _ = _run(L, case, "global", 1002, 0)
-        g1024, _, _ = _run(L, case, "global", 1024, 0)
+        g1002, gl2, gq2 = _run(L, case, "global", 1002, 0)
+        _check(L, case, "global", 1002, 0, g1002, gl2, gq2, rows=[0, 31, 63],
+               name="wl2 global C=1002 M=64 (3 rows)")
+        g1024, gl4, gq4 = _run(L, case, "global", 1024, 0)
+        _check(L, case, "global", 1024, 0, g1024, gl4, gq4, rows=[0, 31, 63],
+               name="wl2 global C=1024 M=64 (3 rows)")
         rep = {}
         for name, cand in (("local_1002", ids), ("global_1002", g1002), ("global_1024", g1024)):
             rep[name] = {f"recall@{k}": float(np.mean([O.recall_at(cand[m], Z[m], k) for m in range(M)]))
@@ -115,9 +153,10 @@ def test_workload3_tree(L):
     case = workload_case(wl, 80)
     ids, lg, q = _run(L, case, "local", wl.T, wl.k_tile)
     assert ids.shape == (80, 1572)
-    _check(case, "local", wl.T, wl.k_tile, ids, lg, q)
+    _check(L, case, "local", wl.T, wl.k_tile, ids, lg, q, name="wl3 tree local 256/2 M=80")
     gi, gl, gq = _run(L, case, "global", wl.C, 0)
-    _check(case, "global", wl.C, 0, gi, gl, gq, rows=[0, 1, 9, 37, 79])
+    _check(L, case, "global", wl.C, 0, gi, gl, gq, rows=[0, 1, 9, 37, 79],
+           name="wl3 tree global C=1024 M=80 (5 rows)")
     h64 = O.bf16_bits_to_f64(case["h"][:16])
     Z = _dense_exact(case["W"], h64)
     rep = {name: {f"recall@{k}": float(np.mean([O.recall_at(c[m], Z[m], k) for m in range(16)]))
@@ -132,7 +171,35 @@ def test_workload4_wide(L, M):
     ids, lg, q = _run(L, case, "local", wl.T, wl.k_tile)
     assert ids.shape == (M, 2376)
     rows = None if M <= 32 else sorted({0, 1, M // 2, M - 1, *range(7, M, M // 6)})
-    _check(case, "local", wl.T, wl.k_tile, ids, lg, q, rows=rows)
+    _check(L, case, "local", wl.T, wl.k_tile, ids, lg, q, rows=rows,
+           name=f"wl4 local 256/4 M={M}" + ("" if rows is None else f" ({len(rows)} rows)"))
+
+
+@pytest.mark.parametrize("index,M", [(2, 16), (3, 80), (4, 8)])
+def test_q_bites_plain_hidden(L, index, M):
+    """q parity where it is not one-hot: hidden states N(0,1) without the
+    W[t] spike, temperature = std of the exact logits over the candidates."""
+    wl = synth.workload(index)
+    case = workload_case(wl, M)
+    case["h"] = synth.make_plain_hidden(wl.d, M, wl.index)
+    T = _candidate_temperature(case, "local", wl.T, wl.k_tile)
+    ids, lg, q = _run(L, case, "local", wl.T, wl.k_tile, temperature=T)
+    _check(L, case, "local", wl.T, wl.k_tile, ids, lg, q, temperature=T,
+           name=f"wl{index} local plain h, T=std(L) M={M}")
+    live = [int((q[m] > P.Q_ABS).sum()) for m in range(M)]
+    assert np.median(live) >= 20, "q is nearly one-hot: the check would not bite"
+
+
+def test_q_bites_recipe_hidden(L):
+    """The spike recipe at T = std(L over candidates) (workload 2, M = 8),
+    local and global."""
+    wl = synth.workload(2)
+    case = workload_case(wl, 8)
+    for mode, C, k in (("local", wl.T, wl.k_tile), ("global", 1024, 0)):
+        T = _candidate_temperature(case, mode, C, k)
+        ids, lg, q = _run(L, case, mode, C, k, temperature=T)
+        _check(L, case, mode, C, k, ids, lg, q, temperature=T,
+               name=f"wl2 {mode} recipe h, T=std(L) M=8")
 
 
 @pytest.mark.parametrize("M", [1, 32])

@@ -340,6 +340,21 @@ def test_recall_is_one_at_full_rank():
         assert O.recall_at(out["ids"][m], Z[m], 8) == 1.0
 
 
+def test_recall_below_one_hand_case():
+    # exact logits rank the ids 0 > 1 > 2 > 3 > 4 > 5; candidates {0, 2, 5}
+    Z = np.array([6.0, 5.0, 4.0, 3.0, 2.0, 1.0])
+    cand = np.array([5, 0, 2])
+    assert O.recall_at(cand, Z, 1) == 1.0          # {0}
+    assert O.recall_at(cand, Z, 2) == 0.5          # {0, 1}: only 0 held
+    assert O.recall_at(cand, Z, 4) == 0.5          # {0, 1, 2, 3}: 0 and 2 held
+    assert abs(O.recall_at(cand, Z, 6) - 0.5) < 1e-15  # 3 of the 6
+    assert O.recall_at(np.array([1, 3]), Z, 1) == 0.0
+    # the exact Top-K breaks ties by the smaller id: ids 1 and 2 tie for second
+    Zt = np.array([9.0, 7.0, 7.0, 1.0])
+    assert O.recall_at(np.array([0, 2]), Zt, 2) == 0.5
+    assert O.recall_at(np.array([0, 1]), Zt, 2) == 1.0
+
+
 def test_local_recall_not_above_global_on_average():
     """At an equal candidate budget the global Top-C holds the C best
     approximate scores, so averaged over many small heads its recall of the
