@@ -27,7 +27,8 @@ __all__ = [
     "GLOBAL", "LOCAL", "LmheadError", "candidate_count", "workspace_size", "project_u",
     "lowrank_score_topk", "gather_logits", "candidate_softmax", "two_stage", "dense_head",
     "pruned_head", "cluster_candidate_count", "cluster_workspace_size", "cluster_two_stage",
-    "draft_select", "verify_chain", "last_device_error", "version", "Workspace",
+    "draft_select", "verify_chain", "last_device_error", "debug_set_wait_cycles", "version",
+    "Workspace",
 ]
 
 _BF16_OK = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (
@@ -223,6 +224,12 @@ def pruned_head(W_pruned: torch.Tensor, h: torch.Tensor, temperature: float = 1.
 def last_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return int(load().lmhead_last_device_error(_stream_ptr(stream)))
+
+
+def debug_set_wait_cycles(cycles: int) -> int:
+    """Test hook: the role-wait budget of the tensor-core kernels in SM cycles
+    (0 = test each wait once, < 0 = the default). Returns the previous one."""
+    return int(load().lmhead_debug_set_wait_cycles(int(cycles)))
 
 
 @functools.lru_cache(maxsize=4096)

@@ -3,16 +3,27 @@
 // allocates device memory or synchronises (except lmhead_last_device_error).
 #include <math.h>
 #include <stdint.h>
+
+#include <atomic>
 #include <stdlib.h>
 #include <string.h>
 
 #include "common.cuh"
 #include "kernels.h"
 #include "lmhead.h"
+#include "tc_util.cuh"
 
 namespace lmhead {
 
 __device__ int g_device_error;
+
+// Role-wait budget of the tensor-core kernels (-1: the default).
+static std::atomic<long long> g_role_wait{-1};
+
+long long role_wait_cycles() {
+  const long long v = g_role_wait.load(std::memory_order_relaxed);
+  return v < 0 ? tc::kWaitCycles : v;
+}
 
 int* device_error_word() {
   static int* cache[64] = {nullptr};
@@ -442,6 +453,12 @@ int lmhead_cluster_two_stage(const lmhead_bf16* W, const lmhead_bf16* A, const l
                              device_error_word(), s, 0);
   if (e == cudaSuccess) e = launch_row_softmax(out_logits, M, K, 1.f / temperature, out_q, s);
   return cuda_status(e);
+}
+
+int64_t lmhead_debug_set_wait_cycles(int64_t cycles) {
+  const long long prev = role_wait_cycles();
+  g_role_wait.store(cycles < 0 ? -1 : (long long)cycles, std::memory_order_relaxed);
+  return prev;
 }
 
 int lmhead_last_device_error(lmhead_stream stream) {

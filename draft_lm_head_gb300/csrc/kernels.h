@@ -88,6 +88,9 @@ cudaError_t launch_verify_chain(const float* p, int64_t n, int B, int Kd, const 
                                 cudaStream_t s);
 
 int* device_error_word();  // this device's error word (nullptr on failure)
+// Budget (SM cycles) of the tensor-core kernels' role waits; tc::kWaitCycles
+// unless lmhead_debug_set_wait_cycles changed it.
+long long role_wait_cycles();
 
 // TMA map of a rows x cols bf16 row-major matrix: box_rows x box_cols
 // (box_cols * 2 == 128 bytes), 128-byte swizzle, zero fill out of bounds.

@@ -41,6 +41,7 @@ constexpr size_t kSmemBudget = 232448 - 2048;
 struct Ctl {
   uint64_t full[kMaxStages], empty[kMaxStages];
   uint64_t acc_full[2], acc_empty[2];
+  uint64_t mma_drain;  // after an abort: the MMA thread's issued MMAs are done
   uint32_t tmem_base;
   int abort;
 };
@@ -62,6 +63,7 @@ struct RowsParams {
   float* out;        // out[m * ldo + row]
   int64_t ldo;
   int* err;
+  long long wait_cycles;  // budget of every role wait (drains keep tc::kWaitCycles)
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -90,6 +92,7 @@ rows_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
       tc::mbar_init(&ctl.acc_full[a], 1);
       tc::mbar_init(&ctl.acc_empty[a], 4);
     }
+    tc::mbar_init(&ctl.mma_drain, 1);
     ctl.abort = 0;
     tc::fence_mbar_init();
   }
@@ -117,7 +120,7 @@ rows_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
           const int kb0 = kg * p.ksub;
           const int nsub = min(p.ksub, p.kblocks - kb0);
           if (it_s >= (uint32_t)NS &&
-              !tc::mbar_wait(&ctl.empty[s], ((it_s / NS) & 1) ^ 1, abort_flag)) {
+              !tc::mbar_wait(&ctl.empty[s], ((it_s / NS) & 1) ^ 1, abort_flag, p.wait_cycles)) {
             ok = false;
             break;
           }
@@ -157,12 +160,12 @@ rows_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
       bool ok = true;
       for (int64_t item = blockIdx.x; item < p.items && ok; item += p.G, ++gq) {
         const int a = (int)(gq & 1);
-        if (!tc::mbar_wait(&ctl.acc_empty[a], ((gq >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(&ctl.acc_empty[a], ((gq >> 1) & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
         tc::fence_after_sync();
         const uint32_t d = tmem + (uint32_t)(a * p.acc_cols);
         for (int kg = 0; kg < p.kgroups; ++kg, ++it_s) {
           const int s = (int)(it_s % NS);
-          if (!tc::mbar_wait(&ctl.full[s], (it_s / NS) & 1, abort_flag)) { ok = false; break; }
+          if (!tc::mbar_wait(&ctl.full[s], (it_s / NS) & 1, abort_flag, p.wait_cycles)) { ok = false; break; }
           tc::fence_after_sync();
           const int kb0 = kg * p.ksub;
           const int nsub = min(p.ksub, p.kblocks - kb0);
@@ -184,6 +187,7 @@ rows_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
       if (!ok) {
         *abort_flag = 1;
         record_error(p.err, kDevErrTimeout);
+        tc::mma_drain(&ctl.mma_drain);  // TMEM is freed below
       }
     }
   } else {
@@ -195,7 +199,7 @@ rows_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
     for (int64_t item = blockIdx.x; item < p.items; item += p.G, ++gq) {
       const int a = (int)(gq & 1);
       int okw = 1;
-      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (gq >> 1) & 1, abort_flag) ? 1 : 0;
+      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (gq >> 1) & 1, abort_flag, p.wait_cycles) ? 1 : 0;
       okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
       if (!okw) {
         if (lane == 0) {
@@ -277,6 +281,7 @@ cudaError_t launch_rows_dense_tc(const bf16_t* X, int64_t n, int kdim, const bf1
   p.out = out;
   p.ldo = ldo;
   p.err = err;
+  p.wait_cycles = role_wait_cycles();
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   p.G = (int)(p.items < (int64_t)sms ? p.items : (int64_t)sms);

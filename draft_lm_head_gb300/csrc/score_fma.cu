@@ -342,12 +342,12 @@ cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_
       return launch_gemv_mb<1, false>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s);
     return launch_gemv_mb<2, true>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s);
   }
+  // the kernel also has ~13 KB of static shared memory, so the opt-in is
+  // needed below 48 KB of dynamic memory too: always raise the limit (cached)
   const size_t smem = (size_t)kMB * r * sizeof(float);
-  if (smem > 48 * 1024) {
-    static int smem_set[64] = {0};
-    cudaError_t e = ensure_dynamic_smem(local_topk_fma_kernel, smem, smem_set);
-    if (e != cudaSuccess) return e;
-  }
+  static int smem_set[64] = {0};
+  cudaError_t e = ensure_dynamic_smem(local_topk_fma_kernel, smem, smem_set);
+  if (e != cudaSuccess) return e;
   dim3 grid((unsigned)tiles, (M + kMB - 1) / kMB);
   return launch_kernel(false, local_topk_fma_kernel, grid, dim3(kThreads), smem, s, A, u, token_ids,
                        n, r, M, T, k_tile, K, out_ids, out_scores);

@@ -56,6 +56,7 @@ struct SharedCtl {
   uint64_t ufull;
   uint64_t acc_full[kAcc];
   uint64_t acc_empty[kAcc];
+  uint64_t mma_drain;  // after an abort: the MMA thread's issued MMAs are done
   uint32_t tmem_base;
   int abort;
   int decision[2];
@@ -75,6 +76,7 @@ struct Params {
   float2* partials;   // [HC][G][2][kHid][KT]
   int* tile_tickets;  // [HC][tiles]
   int* err;
+  long long wait_cycles;  // budget of every role wait (drains keep tc::kWaitCycles)
 };
 
 __device__ __forceinline__ int32_t vocab_id(const Params& p, int64_t pos) {
@@ -199,6 +201,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       tc::mbar_init(&ctl.acc_full[a], 1);
       tc::mbar_init(&ctl.acc_empty[a], 4);
     }
+    tc::mbar_init(&ctl.mma_drain, 1);
     ctl.abort = 0;
     tc::fence_mbar_init();
   }
@@ -237,7 +240,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       for (int i = (int)(it / kblocks); i < nch && ok; ++i) {
         for (int kb = (i == (int)(it / kblocks)) ? (int)(it % kblocks) : 0; kb < kblocks; ++kb, ++it) {
           const int s = (int)(it % NS);
-          if (!tc::mbar_wait(&ctl.empty[s], ((it / NS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          if (!tc::mbar_wait(&ctl.empty[s], ((it / NS) & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(&ctl.full[s], kStageBytes);
           tc::tma_load_2d(stage_s + (size_t)s * kStageBytes, &amap, &ctl.full[s], kb * kKBlock,
                           (int)((c0 + i) * kChunk));
@@ -264,16 +267,16 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = tc::mbar_wait(&ctl.ufull, 0, abort_flag);
+      bool ok = tc::mbar_wait(&ctl.ufull, 0, abort_flag, p.wait_cycles);
       uint32_t it = 0;
       for (int i = 0; i < nch && ok; ++i) {
         const int a = i % kAcc;
-        if (!tc::mbar_wait(&ctl.acc_empty[a], ((i / kAcc) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(&ctl.acc_empty[a], ((i / kAcc) & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
         tc::fence_after_sync();
         const uint32_t d = tmem + a * kChunk;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = (int)(it % NS);
-          if (!tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag)) { ok = false; break; }
+          if (!tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag, p.wait_cycles)) { ok = false; break; }
           tc::fence_after_sync();
           const uint64_t adesc = tc::sw128_kmajor_desc(tc::smem_addr(u_s + (size_t)kb * kStageBytes));
           const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_addr(stage_s + (size_t)s * kStageBytes));
@@ -288,6 +291,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
       if (!ok) {
         *abort_flag = 1;
         record_error(p.err, kDevErrTimeout);
+        tc::mma_drain(&ctl.mma_drain);  // TMEM is freed below
       }
     }
   } else {
@@ -335,7 +339,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
         const int a = i % kAcc;
         int okw = 1;
         if (lane == 0) {
-          okw = ok && tc::mbar_wait(&ctl.acc_full[a], (i / kAcc) & 1, abort_flag) ? 1 : 0;
+          okw = ok && tc::mbar_wait(&ctl.acc_full[a], (i / kAcc) & 1, abort_flag, p.wait_cycles) ? 1 : 0;
           if (!okw) *abort_flag = 1;
         }
         okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
@@ -404,7 +408,7 @@ local_topk_tc_kernel(const __grid_constant__ CUtensorMap amap,
     for (int i = 0; i < nch; ++i) {
       const int a = i % kAcc;
       int okw = 1;
-      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (i / kAcc) & 1, abort_flag) ? 1 : 0;
+      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (i / kAcc) & 1, abort_flag, p.wait_cycles) ? 1 : 0;
       okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
       if (!okw) { ok = false; break; }
       tc::fence_after_sync();
@@ -591,6 +595,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
       tc::mbar_init(&ctl.acc_full[a], 1);
       tc::mbar_init(&ctl.acc_empty[a], 4);
     }
+    tc::mbar_init(&ctl.mma_drain, 1);
     ctl.abort = 0;
     tc::fence_mbar_init();
   }
@@ -634,7 +639,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
         const int slot = c % kDescRing;
         if (tile < 0 || tile >= p.tiles) {  // no more work: an end marker through the ring
           const int s = (int)(it % NS);
-          if (it >= (uint32_t)NS && !tc::mbar_wait(&ctl.empty[s], ((it / NS) & 1) ^ 1, abort_flag)) {
+          if (it >= (uint32_t)NS && !tc::mbar_wait(&ctl.empty[s], ((it / NS) & 1) ^ 1, abort_flag, p.wait_cycles)) {
             ok = false;
             break;
           }
@@ -661,7 +666,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
             for (int g2 = 0; g2 < gcount; ++g2) {
               const uint32_t itg = it + (uint32_t)g2;
               if (itg >= (uint32_t)NS &&
-                  !tc::mbar_wait(&ctl.empty[itg % NS], ((itg / NS) & 1) ^ 1, abort_flag)) {
+                  !tc::mbar_wait(&ctl.empty[itg % NS], ((itg / NS) & 1) ^ 1, abort_flag, p.wait_cycles)) {
                 ok = false;
                 break;
               }
@@ -705,16 +710,16 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = tc::mbar_wait(&ctl.ufull, 0, abort_flag);
+      bool ok = tc::mbar_wait(&ctl.ufull, 0, abort_flag, p.wait_cycles);
       uint32_t it = 0;
       for (int c = 0; ok; ++c) {
         const int a = c % kNAcc;
         int s = (int)(it % NS);
-        if (!tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag, p.wait_cycles)) { ok = false; break; }
         // the slot must be free before anything, the end marker included, is
         // signalled on it: an arrival two phases ahead of the epilogue's wait
         // would hide the phase it waits for
-        if (!tc::mbar_wait(&ctl.acc_empty[a], ((c / kNAcc) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(&ctl.acc_empty[a], ((c / kNAcc) & 1) ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
         if (desc_tile[c % kDescRing] < 0) {  // end marker: pass it on to the epilogue
           tc::mbar_arrive(&ctl.acc_full[a]);
           break;
@@ -723,7 +728,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
         const uint32_t d = tmem + a * CH;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           s = (int)(it % NS);
-          if (kb > 0 && !tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag)) { ok = false; break; }
+          if (kb > 0 && !tc::mbar_wait(&ctl.full[s], (it / NS) & 1, abort_flag, p.wait_cycles)) { ok = false; break; }
           tc::fence_after_sync();
           const uint64_t adesc = tc::sw128_kmajor_desc(tc::smem_addr(u_s + (size_t)kb * kStageBytes));
           const uint64_t bdesc = tc::sw128_kmajor_desc(tc::smem_addr(stage_s + (size_t)s * kSt));
@@ -738,6 +743,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
       if (!ok) {
         *abort_flag = 1;
         record_error(p.err, kDevErrTimeout);
+        tc::mma_drain(&ctl.mma_drain);  // TMEM is freed below
       }
     }
   } else {
@@ -762,7 +768,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
     for (int c = 0;; ++c) {
       const int a = c % kNAcc;
       int okw = 1;
-      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (c / kNAcc) & 1, abort_flag) ? 1 : 0;
+      if (lane == 0) okw = tc::mbar_wait(&ctl.acc_full[a], (c / kNAcc) & 1, abort_flag, p.wait_cycles) ? 1 : 0;
       okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
       if (!epilogue_all(okw != 0)) {  // uniform: every epilogue warp leaves together
         if (lane == 0) { *abort_flag = 1; record_error(p.err, kDevErrTimeout); }
@@ -934,6 +940,7 @@ cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t
   p.partials = static_cast<float2*>(partials);
   p.tile_tickets = tile_tickets;
   p.err = err;
+  p.wait_cycles = role_wait_cycles();
   CUtensorMap amap, umap;
   if (!make_bf16_map(&amap, A, (uint64_t)n, (uint64_t)r, ch, kKBlock) ||
       !make_bf16_map(&umap, u, (uint64_t)M, (uint64_t)r, p.rows_per_rep, kKBlock))

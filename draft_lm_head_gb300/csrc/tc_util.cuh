@@ -52,13 +52,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Test the phase once, without suspending the thread.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `parity` to complete. Returns false if the wait ran
-// out (kWaitCycles) or another role raised `abort`.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// out (`budget` SM clock cycles; a budget of 0 or less tests the phase once
+// and gives up unless it is already complete) or another role raised
+// `abort`.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          long long budget = kWaitCycles) {
+  if (budget <= 0) return mbar_test(bar, parity);
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > budget) return false;
   }
   return true;
 }
@@ -115,6 +132,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_addr(bar))
       : "memory");
+}
+
+// After an abort: wait (bounded by kWaitCycles) until every tcgen05
+// operation this thread issued has completed, so TMEM is not freed under an
+// MMA still in flight. `bar` is a fresh barrier (count 1) used once.
+__device__ __forceinline__ void mma_drain(uint64_t* bar) {
+  mma_commit(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, 0) && clock64() - t0 < kWaitCycles) {
+  }
 }
 
 // 32 lanes x 32 consecutive fp32 columns: thread i gets lane (base + i).

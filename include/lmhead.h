@@ -205,6 +205,12 @@ int lmhead_pruned_head(const lmhead_bf16* W_pruned, const lmhead_bf16* h, int n_
  * forbids allocation in its decode loop, or C/C++ code embedding the library
  * with no device allocator of its own. Arguments, outputs and results are
  * those of lmhead_two_stage with mode = LMHEAD_LOCAL, C_or_tile = T.
+ *   Speed: it always scores on CUDA cores (the warp-per-row GEMV kernel for
+ *   one or two hidden vectors at r = 256, otherwise the CUDA-core tile
+ *   kernel), because the tensor-core scoring needs scratch that grows with M
+ *   and n. At one or two hidden vectors it runs the same kernels as
+ *   lmhead_two_stage; at larger M (the 64-vector batch of the 128256-row head,
+ *   say) it is several times slower than lmhead_two_stage.
  *   Scratch: a fixed static device array of 513 KiB (u for M <= 256 and
  *   r <= 1024, plus M per-row counters) held by every GPU that loads the
  *   library until the process exits. M > 256, r > 1024 or k_tile > 32
@@ -307,6 +313,24 @@ int lmhead_verify_chain(const float* p, int64_t n, int B, int Kd, const int32_t*
                         const int32_t* cand_ids, const float* cand_q, int K, const float* r,
                         const float* u, int32_t* out_tokens, int32_t* out_count,
                         lmhead_stream stream);
+
+/*
+ * Test hook for the timeout path (the pages have no counterpart). Every wait
+ * between the warp roles of the tensor-core kernels (the fused score + tile
+ * top-k, the global path's score writeback, the dense and pruned heads) is
+ * bounded by a budget of SM clock cycles, about a second by default; on
+ * expiry the kernel records LMHEAD_ERR_TIMEOUT in the device error word,
+ * waits for its own copies and MMAs in flight, frees its tensor memory and
+ * returns, leaving that call's outputs undefined and the context usable.
+ *   cycles > 0   sets the budget for kernels launched from now on;
+ *   cycles == 0  makes each such wait test its barrier once and give up
+ *                unless it is already complete (a call then almost surely
+ *                times out: this is how the tests exercise the path);
+ *   cycles < 0   restores the default.
+ * Process-wide, read at launch (a captured CUDA graph keeps the budget of its
+ * capture). Returns the previous budget. Not meant for production use.
+ */
+int64_t lmhead_debug_set_wait_cycles(int64_t cycles);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error

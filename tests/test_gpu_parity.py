@@ -283,6 +283,23 @@ def test_local_gemv_small_batches(L, M, T, k):
     P.check_q(host(q), ex)
 
 
+@pytest.mark.parametrize("M", [1, 9])
+def test_local_wide_rank_cuda_cores(L, M):
+    # r = 1280 is beyond the tensor-core scoring (r <= 512): the CUDA-core
+    # kernel holds u (8 x r fp32 = 40 KB) next to ~13 KB of static shared
+    # memory, over the 48 KB default
+    case = make_case(3000, 1536, 1280, M, seed=19, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    ids, lg, q = L.two_stage(L.LOCAL, W, A, B, h, tok, 256, 4)
+    assert L.last_device_error() == 0
+    _, S, h64, SL = oracle_scores(case, with_slack=True)
+    ids = host(ids)
+    P.check_ids("local", ids, S, case["tok"], 256, 4, slack_pos=SL)
+    ex = P.exact_logits(case["W"], h64, ids)
+    P.check_logits(host(lg), ex)
+    P.check_q(host(q), ex)
+
+
 @pytest.mark.parametrize("M", [1, 17, 300])
 def test_dense_head_blocks(L, M):
     # tensor cores at every M (N = M hidden vectors per MMA, M > 256 in blocks

@@ -51,6 +51,26 @@ def test_check_u_accepts_only_ambiguous_neighbours():
         raise AssertionError("a flip of an unambiguous element passed")
 
 
+def test_check_u_under_cancellation():
+    # exact u = 2^-20, but the fp32 error bound (15 roundings of |terms| ~ 2)
+    # is ~1.8e-6: any bf16 value the interval [x - e, x + e] rounds to is right
+    h = np.array([[1.0, 1.0, 1.0]])
+    B = np.array([[1.0, -1.0, 2.0 ** -20]])
+    e = P.u_gamma(3, 1) * (2.0 + 2.0 ** -20)
+    assert e > 2.0 ** -20
+    assert P.check_u(_bits(2.0 ** -19)[None], B, h) == (1, 1)
+    assert P.check_u(_bits(0.0)[None], B, h) == (1, 1)
+    for wrong in (2.0 ** -17, -(2.0 ** -19)):
+        try:
+            P.check_u(_bits(wrong)[None], B, h)
+        except AssertionError:
+            pass
+        else:
+            raise AssertionError("a value outside the error interval passed")
+    sl = P.u_slack(np.array([[1.0]]), B, h)
+    assert e - 2.0 ** -26 <= sl[0, 0] <= e + 2.0 ** -26   # both ends rounded to bf16
+
+
 def test_u_slack_counts_only_ambiguous_elements():
     h = np.array([[1.0, 1.0, 1.0]])
     B = np.array([[1.0, 2.0 ** -8, 2.0 ** -30],     # ambiguous (ulp 2^-7)
