@@ -45,7 +45,10 @@ def parse():
     p.add_argument("--M", type=int, default=64)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the per-configuration table (configs 1-4, all modes and heads)")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--cpu-sample", type=int, default=-1, help=argparse.SUPPRESS)
     p.add_argument("--rotations", type=int, default=NROT,
                    help="input copies cycled through (>= 4 keeps every read cold in L2)")
     return p.parse_args()
@@ -116,6 +119,37 @@ def peaks():
             pk = json.load(fh)
         return float(pk["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def pstats(xs):
+    """median, p10 and p90 of a list of per-call times (us)."""
+    xs = sorted(xs)
+    n = len(xs)
+
+    def q(p):
+        return xs[min(n - 1, int(round(p * (n - 1))))]
+    return {"median": round(statistics.median(xs), 2), "p10": round(q(0.1), 2),
+            "p90": round(q(0.9), 2), "calls": n}
+
+
+def per_call_us(torch, fns, reps=100, warm=20, graph=False):
+    """Device time of each of `reps` calls, with events around each call on
+    the current stream; call i runs fns[i % len(fns)] (one per input copy, so
+    consecutive calls read different copies: cold L2). graph=True replays a
+    CUDA graph of the same call instead of launching it from the host."""
+    run = [g.replay for g in (make_graph(torch, f) for f in fns)] if graph else fns
+    n = len(run)
+    for i in range(max(warm, n)):
+        run[i % n]()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for i, (a, b) in enumerate(ev):
+        a.record()
+        run[i % n]()
+        b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e3 for a, b in ev]
 
 
 # ---------------------------------------------------------------- clocks
@@ -333,6 +367,211 @@ def time_cluster(torch, L, head, rot_h, hbm, group=128, G=8, reps=40):
     return res
 
 
+# ---------------------------------------------------------------- every configuration
+# (workload, kind, mode, C_or_tile, k_tile, M values): configuration 1 is the
+# global path on the unshuffled head, 2 the headline head (local, and global
+# at the local candidate count and at 1024), 3 the draft-tree head, 4 the wide
+# head; the dense full-vocabulary head beside each, and the 32000-row
+# frequency-pruned head on the wide one.
+CONFIG_PLAN = (
+    (1, "two_stage", "global", 1024, 0, (1, 4, 8)),
+    (2, "two_stage", "local", 256, 2, (1, 8, 16, 32, 64)),
+    (2, "two_stage", "global", 1002, 0, (1, 8, 16, 32, 64)),
+    (2, "two_stage", "global", 1024, 0, (1, 8, 16, 32, 64)),
+    (2, "dense", None, 0, 0, (1, 4, 8, 16, 32, 64)),
+    (3, "two_stage", "local", 256, 2, (80,)),
+    (3, "two_stage", "global", 1024, 0, (80,)),
+    (3, "dense", None, 0, 0, (80,)),
+    (4, "two_stage", "local", 256, 4, (1, 8, 32, 128, 512)),
+    (4, "dense", None, 0, 0, (1, 8, 32, 128, 512)),
+    (4, "pruned", None, 32000, 0, (1, 8, 32, 128, 512)),
+)
+
+
+def config_hidden(wl, W, M):
+    if wl.tree:
+        h, _ = synth.make_tree_hidden(W, M // len(synth.TREE_PARENT), wl.index)
+    else:
+        h, _ = synth.make_hidden(W, M, wl.index)
+    return h
+
+
+def time_configs(torch, L, hbm, reps=100):
+    """Per-call latency of every configuration: stream-launched and CUDA-graph
+    replayed (median, p10, p90 over `reps` calls rotating over NROT copies of
+    every input), hidden vecs/s and the whole call's HBM fraction from the
+    graph median, with the algorithmic bytes (2nr + 2rd + 2Md + 2dU + 12MK for
+    the two-stage head, U the distinct candidate rows; 2nd + 2Md + 12Mn for the
+    dense head, softmax included; the same over the kept rows for the pruned
+    head)."""
+    from draft_lm_head_gb300 import prep
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    rows = []
+    for idx in sorted({p[0] for p in CONFIG_PLAN}):
+        wl = synth.workload(idx)
+        head = head_inputs(wl)
+        n, d, r = wl.n, wl.d, wl.r
+        W0, A0, B0 = dev(head["W"]), dev(head["A"]), dev(head["B"])
+        tok0 = torch.from_numpy(np.ascontiguousarray(head["tok"], dtype=np.int32)).cuda()
+        rot = [(W0, A0, B0, tok0)] + [(W0.clone(), A0.clone(), B0.clone(), tok0.clone())
+                                      for _ in range(NROT - 1)]
+        pruned = None
+        ws = L.Workspace()
+        for (ci, kind, mode, C, k, Ms) in CONFIG_PLAN:
+            if ci != idx:
+                continue
+            if kind == "pruned" and pruned is None:
+                Wp, _ = prep.pruned_rows(head["W"], head["counts"], C)
+                pruned = [dev(Wp) for _ in range(NROT)]
+            for M in Ms:
+                hb = config_hidden(wl, head["W"], M)
+                hs = [dev(hb) for _ in range(NROT)]
+                ent = {"config": idx, "head": kind, "M": M}
+                if kind == "two_stage":
+                    md = L.LOCAL if mode == "local" else L.GLOBAL
+                    K = L.candidate_count(md, n, C, k)
+                    outs = [(torch.empty((M, K), dtype=torch.int32, device="cuda"),
+                             torch.empty((M, K), dtype=torch.float32, device="cuda"),
+                             torch.empty((M, K), dtype=torch.float32, device="cuda"))
+                            for _ in range(NROT)]
+                    fns = [lambda j=j: L.two_stage(md, rot[j][0], rot[j][1], rot[j][2], hs[j],
+                                                   rot[j][3], C, k, workspace=ws, out=outs[j])
+                           for j in range(NROT)]
+                    ent.update({"mode": mode, "candidates": K})
+                    ent.update({"tile": C, "k_tile": k} if mode == "local" else {"C": C})
+                elif kind == "dense":
+                    lg = torch.empty((M, n), dtype=torch.float32, device="cuda")
+                    q = torch.empty((M, n), dtype=torch.float32, device="cuda")
+                    fns = [lambda j=j: L.dense_head(rot[j][0], hs[j], out=(lg, q))
+                           for j in range(NROT)]
+                else:
+                    lg = torch.empty((M, C), dtype=torch.float32, device="cuda")
+                    q = torch.empty((M, C), dtype=torch.float32, device="cuda")
+                    fns = [lambda j=j: L.pruned_head(pruned[j], hs[j], out=(lg, q))
+                           for j in range(NROT)]
+                    ent["kept_rows"] = C
+                st = pstats(per_call_us(torch, fns, reps))
+                gr = pstats(per_call_us(torch, fns, reps, graph=True))
+                if kind == "two_stage":
+                    U = int(np.unique(outs[0][0].cpu().numpy()).size)
+                    by = 2 * n * r + 2 * r * d + 2 * M * d + 2 * d * U + 12 * M * K
+                    ent["unique_rows"] = U
+                elif kind == "dense":
+                    by = 2 * n * d + 2 * M * d + 12 * M * n
+                else:
+                    by = 2 * C * d + 2 * M * d + 12 * M * C
+                us = gr["median"]
+                ent.update({"stream_us": st, "graph_us": gr, "us": us,
+                            "vecs_per_s": round(M / us * 1e6, 1), "bytes": by,
+                            "hbm_frac": round(by / (us * 1e-6) / 1e9 / hbm, 4)})
+                rows.append(ent)
+                del fns, hs
+        del rot, pruned
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return rows
+
+
+def dense_speedups(rows):
+    """Two-stage vs dense latency (graph medians) per configuration and M."""
+    dense = {(e["config"] if e["config"] != 1 else 2, e["M"]): e["us"]
+             for e in rows if e["head"] == "dense"}
+    out = []
+    for e in rows:
+        if e["head"] != "two_stage":
+            continue
+        key = (e["config"] if e["config"] != 1 else 2, e["M"])
+        if key in dense:
+            out.append({"config": e["config"], "mode": e["mode"], "M": e["M"],
+                        "two_stage_us": e["us"], "dense_us": dense[key],
+                        "speedup": round(dense[key] / e["us"], 2)})
+    return out
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+CPU_MODES = {0: ("local", 128, 4), 1: ("global", 1024, 0), 2: ("local", 256, 2),
+             3: ("local", 256, 2), 4: ("local", 256, 4)}
+
+
+def oracle_config_rate(idx, budget_s=2.5):
+    """The oracle as it stands on configuration idx: steps u -> scores ->
+    Top-k -> logits -> q for one hidden vector at a time (the configuration's
+    first M rows in turn), repeated for about budget_s. Returns a record."""
+    import oracle as O
+    wl = synth.workload(idx)
+    mode, C, k = CPU_MODES[idx]
+    head = head_inputs(wl)
+    A64 = O.bf16_bits_to_f64(head["A"])
+    B64 = O.bf16_bits_to_f64(head["B"])
+    tok = head["tok"]
+    h64 = O.bf16_bits_to_f64(config_hidden(wl, head["W"], max(wl.Ms)))
+    done, t0 = 0, time.perf_counter()
+    while True:
+        hm = h64[done % h64.shape[0]][None]
+        u = O.project_u(B64, hm)
+        S = O.lowrank_scores(A64, u)[0]
+        ids = O.local_topk(S, tok, C, k)[0] if mode == "local" else O.global_topk(S, tok, C)[0]
+        Lg = O.candidate_logits(O.bf16_bits_to_f64(head["W"][ids]), hm[0], np.arange(ids.size))
+        O.candidate_softmax(Lg)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"config": idx, "mode": mode, "vecs_per_s": round(done / dt, 3),
+            "us_per_vec": round(dt / done * 1e6, 1), "vectors": done}
+
+
+def cpu_configs():
+    """Oracle rates per configuration: all host cores for configurations 0-4,
+    one thread (BLAS pinned to one thread in a child process) for 0-2."""
+    cores = len(os.sched_getaffinity(0))
+    out = []
+    for idx in range(5):
+        rec = oracle_config_rate(idx)
+        rec["threads"] = cores
+        out.append(rec)
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    for idx in range(3):
+        p = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", str(idx)],
+                           capture_output=True, text=True, env=env, timeout=300)
+        if p.returncode == 0 and p.stdout.strip():
+            rec = json.loads(p.stdout.strip().splitlines()[-1])
+            rec["threads"] = 1
+            out.append(rec)
+    return out
+
+
+def parity_sample(head, hb, out, rows=(0, 31, 63)):
+    """Parity of the timed call on a few of its rows against the oracle
+    (the boundary rule of the candidate ids, the logits and q tolerances):
+    counts of excused ids inside the 1e-3 band and needing the u-rounding
+    slack, and the largest logit and q errors."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle as O
+    import parity as P
+    wl = WORKLOAD
+    ids, lg, q = (t.cpu().numpy() for t in out)
+    M = ids.shape[0]
+    rows = [m for m in rows if m < M]
+    A64 = O.bf16_bits_to_f64(head["A"])
+    B64 = O.bf16_bits_to_f64(head["B"])
+    h64 = O.bf16_bits_to_f64(hb[rows])
+    S = O.lowrank_scores(A64, O.project_u(B64, h64))
+    SL = P.u_slack(A64, B64, h64, M_call=M)
+    counts = P.check_ids("local", ids[rows], S, head["tok"], wl.T, wl.k_tile, slack_pos=SL)
+    ex = P.exact_logits(head["W"], h64, ids[rows])
+    P.check_logits(lg[rows], ex)
+    P.check_q(q[rows], ex)
+    rel = np.abs(lg[rows] - ex) / np.maximum(np.abs(ex), 1.0)
+    qerr = max(float(np.abs(q[m] - O.candidate_softmax(ex[i])).max()) for i, m in enumerate(rows))
+    return {"rows": rows, "ids_compared": counts["compared"], "excused_band": counts["band"],
+            "excused_slack": counts["slack"], "logit_max_rel_err": float(rel.max()),
+            "q_max_abs_err": qerr, "passed": True}
+
+
 def run_ours(args):
     import ctypes
     global NROT
@@ -548,19 +787,30 @@ def run_ours(args):
                           "hbm_frac": round(by / (us * 1e-6) / 1e9 / hbm, 4),
                           "dense_us": round(dus, 2)})
             del g, gd
+    # per-call latency of the headline call: stream-launched and graph-replayed
+    lat = {"stream": pstats(per_call_us(torch, [lambda j=j: step(j) for j in range(NROT)], 200)),
+           "graph": pstats(per_call_us(torch, [lambda j=j: step(j) for j in range(NROT)], 200,
+                                       graph=True))}
     # the steps after q (draft selection, chain verification), for context
     after_q = {}
     cluster = []
     if not args.no_sweep and rank == 0:
         after_q = time_after_q(torch, L, outs[0], hbm)
         cluster = time_cluster(torch, L, head, rot, hbm)
+    configs = []
+    if not args.no_configs and rank == 0:
+        configs = time_configs(torch, L, hbm)
     clocks = sampler.stop()
 
     cpu = None
+    parity = None
     if rank == 0 and not args.no_cpu:
         rate, cores, sample = oracle_sample_rate(head, hb)
         cpu = {"value": round(rate, 3), "unit": "hidden vecs/s", "cores": cores, "kind": "oracle",
                "sample": sample}
+        parity = parity_sample(head, hb, outs[0])
+        if not args.no_configs:
+            cpu["per_config"] = cpu_configs()
 
     if rank == 0:
         line = {
@@ -573,7 +823,9 @@ def run_ours(args):
             "clocks": clocks, "kernel_us": {k: round(v, 3) for k, v in kern_us.items()},
             "step_bytes": step_bytes,
             "step_hbm_frac": round(step_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm, 4),
-            "unique_rows": U, "sweep": sweep, "after_q": after_q, "cluster_route": cluster,
+            "unique_rows": U, "latency_us": lat, "parity_counts": parity, "sweep": sweep,
+            "configs": configs, "vs_dense": dense_speedups(configs), "after_q": after_q,
+            "cluster_route": cluster,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -631,6 +883,9 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.cpu_sample >= 0:  # child of cpu_configs: one oracle rate, one JSON line
+        print(json.dumps(oracle_config_rate(args.cpu_sample)), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -26,7 +26,7 @@ from typing import Optional
 
 import numpy as np
 
-__all__ = ["smoothed_frequency", "freq_aware_factors", "bf16_bits"]
+__all__ = ["smoothed_frequency", "freq_aware_factors", "bf16_bits", "pruned_rows"]
 
 
 def smoothed_frequency(counts: np.ndarray) -> np.ndarray:
@@ -69,3 +69,18 @@ def freq_aware_factors(W_bits: np.ndarray, counts: np.ndarray, r: int,
         A[r0:r0 + rows.size] = bf16_bits(_bits_to_f64(W_bits[rows]) @ V)
     B = bf16_bits(V.T)
     return {"A": A, "B": B, "token_ids": token_ids, "eigenvalues": evals[order]}
+
+
+def pruned_rows(W_bits: np.ndarray, counts: np.ndarray, n_keep: int = 32000):
+    """The comparison head of the EAGLE-4 notes' "EAGLE Efficient LM Head"
+    section that keeps only the n_keep most frequent tokens (32000 there),
+    built offline: returns (W_pruned, kept), kept the vocabulary ids in
+    ascending order (ties in frequency go to the smaller id) and W_pruned
+    their rows of W copied contiguously (the layout lmhead_pruned_head
+    takes; output column j belongs to kept[j])."""
+    n = W_bits.shape[0]
+    if not 1 <= n_keep <= n:
+        raise ValueError(f"n_keep={n_keep} must be in [1, n={n}]")
+    f = smoothed_frequency(counts)
+    kept = np.sort(np.argsort(-f, kind="stable")[:n_keep]).astype(np.int64)
+    return np.ascontiguousarray(W_bits[kept]), kept

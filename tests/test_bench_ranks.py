@@ -74,3 +74,30 @@ def test_workload_config_names_the_headline_workload():
     assert c["candidates"] == 1002 == (128256 // 256) * 2
     assert c["parallelism"] == "replicas x2 (independent hidden vectors)"
     assert "> 2x L2" in c["l2"] and "> 2x L2" not in bench.workload_config(64, 1, 1)["l2"]
+
+
+def test_pstats_percentiles():
+    s = bench.pstats([float(x) for x in range(1, 102)])      # 1 .. 101
+    assert (s["median"], s["p10"], s["p90"], s["calls"]) == (51.0, 11.0, 91.0, 101)
+
+
+def test_dense_speedups_pair_by_head_and_M():
+    rows = [{"config": 1, "head": "two_stage", "mode": "global", "M": 4, "us": 50.0},
+            {"config": 2, "head": "two_stage", "mode": "local", "M": 4, "us": 25.0},
+            {"config": 2, "head": "dense", "M": 4, "us": 175.0},
+            {"config": 4, "head": "two_stage", "mode": "local", "M": 8, "us": 40.0},
+            {"config": 4, "head": "dense", "M": 8, "us": 300.0},
+            {"config": 4, "head": "pruned", "M": 8, "us": 60.0}]
+    out = {(e["config"], e["M"]): e["speedup"] for e in bench.dense_speedups(rows)}
+    # configurations 1 and 2 share a head, so share its dense timing
+    assert out == {(1, 4): 3.5, (2, 4): 7.0, (4, 8): 7.5}
+
+
+def test_config_plan_covers_every_named_configuration():
+    plan = {(c, kind, mode, C, k): Ms for c, kind, mode, C, k, Ms in bench.CONFIG_PLAN}
+    assert plan[(1, "two_stage", "global", 1024, 0)] == (1, 4, 8)
+    assert plan[(2, "two_stage", "local", 256, 2)] == (1, 8, 16, 32, 64)
+    assert {(3, "two_stage", "local", 256, 2), (3, "two_stage", "global", 1024, 0)} <= set(plan)
+    assert plan[(4, "two_stage", "local", 256, 4)] == (1, 8, 32, 128, 512)
+    assert plan[(4, "pruned", None, 32000, 0)] == (1, 8, 32, 128, 512)
+    assert set(plan[(2, "dense", None, 0, 0)]) >= {1, 4, 8, 16, 32, 64}

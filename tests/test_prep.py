@@ -35,3 +35,14 @@ def test_prep_identity_order_and_full_rank():
     AB = O.bf16_bits_to_f64(fac["A"]) @ O.bf16_bits_to_f64(fac["B"])
     W64 = O.bf16_bits_to_f64(W)
     assert np.linalg.norm(AB - W64) / np.linalg.norm(W64) < 1e-2
+
+
+def test_pruned_rows_match_the_oracle():
+    import synth
+    rng = np.random.default_rng(3)
+    counts = rng.integers(0, 50, 400)          # many ties
+    W = synth.make_head(400, 16, 0)
+    Wp, kept = prep.pruned_rows(W, counts, 123)
+    want = O.pruned_ids(O.smooth_freq(counts), 123)
+    assert np.array_equal(kept, want)
+    assert np.array_equal(Wp, W[want])
