@@ -28,7 +28,7 @@ __all__ = [
     "lowrank_score_topk", "gather_logits", "candidate_softmax", "two_stage", "dense_head",
     "pruned_head", "cluster_candidate_count", "cluster_workspace_size", "cluster_two_stage",
     "draft_select", "verify_chain", "last_device_error", "debug_set_wait_cycles", "version",
-    "Workspace",
+    "Workspace", "shard_workspace_size", "shard_two_stage", "shard_softmax",
 ]
 
 _BF16_OK = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (
@@ -219,6 +219,57 @@ def pruned_head(W_pruned: torch.Tensor, h: torch.Tensor, temperature: float = 1.
                                     _typed(q, torch.float32, "q"), _stream_ptr(stream)),
           "pruned_head")
     return L, q
+
+
+def shard_workspace_size(n_shard: int, d: int, r: int, M: int, T: int, k_tile: int) -> int:
+    return int(load().lmhead_shard_workspace_size(n_shard, d, r, M, T, k_tile))
+
+
+def shard_two_stage(W_shard: torch.Tensor, A_shard: torch.Tensor, B: torch.Tensor,
+                    h: torch.Tensor, token_ids_shard: torch.Tensor, row_of_id: torch.Tensor,
+                    T: int, k_tile: int, temperature: float = 1.0, workspace=None, out=None,
+                    stream=None):
+    """One vocabulary shard of the local head (see lmhead_shard_two_stage):
+    returns (ids, logits, stats), stats M x 2 (max, sum of exponentials)."""
+    n_shard, r = A_shard.shape
+    d = B.shape[1]
+    M = h.shape[0]
+    n_vocab = row_of_id.shape[0]
+    K = candidate_count(LOCAL, n_shard, T, k_tile)
+    dev = h.device
+    if out is None:
+        ids = torch.empty((M, K), dtype=torch.int32, device=dev)
+        L = torch.empty((M, K), dtype=torch.float32, device=dev)
+        stats = torch.empty((M, 2), dtype=torch.float32, device=dev)
+    else:
+        ids, L, stats = out
+    _check_shapes(A_shard.device, W_shard=(W_shard, (n_shard, d)), B=(B, (r, d)), h=(h, (M, d)),
+                  token_ids_shard=(token_ids_shard, (n_shard,)), ids=(ids, (M, K)),
+                  logits=(L, (M, K)), stats=(stats, (M, 2)))
+    nbytes = shard_workspace_size(n_shard, d, r, M, T, k_tile)
+    ws = _ws(workspace, nbytes, dev)
+    check(load().lmhead_shard_two_stage(
+        _bf16(W_shard, "W_shard"), _bf16(A_shard, "A_shard"), _bf16(B, "B"), _bf16(h, "h"),
+        _typed(token_ids_shard, torch.int32, "token_ids_shard"),
+        _typed(row_of_id, torch.int32, "row_of_id"), n_vocab, n_shard, d, r, M, T, k_tile,
+        float(temperature), _typed(ids, torch.int32, "ids"), _typed(L, torch.float32, "logits"),
+        _typed(stats, torch.float32, "stats"), ws.data_ptr(), ws.numel(), _stream_ptr(stream)),
+        "shard_two_stage")
+    return ids, L, stats
+
+
+def shard_softmax(all_stats: torch.Tensor, logits: torch.Tensor, temperature: float = 1.0,
+                  out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """q of one shard's candidates from every shard's stats (G x M x 2)."""
+    M, K = logits.shape
+    G = all_stats.shape[0]
+    _check_shapes(logits.device, all_stats=(all_stats, (G, M, 2)), out=(out, (M, K)))
+    q = out if out is not None else torch.empty_like(logits)
+    check(load().lmhead_shard_softmax(
+        _typed(all_stats, torch.float32, "all_stats"), G, _typed(logits, torch.float32, "logits"),
+        M, K, float(temperature), _typed(q, torch.float32, "out"), _stream_ptr(stream)),
+        "shard_softmax")
+    return q
 
 
 def last_device_error(stream=None) -> int:

@@ -33,6 +33,10 @@ SIGNATURES = {
     "lmhead_pruned_head": (_I, [_P, _P, _I, _I, _I, _F, _P, _P, _P]),
     "lmhead_last_device_error": (_I, [_P]),
     "lmhead_debug_set_wait_cycles": (_I64, [_I64]),
+    "lmhead_shard_workspace_size": (_SZ, [_I64, _I, _I, _I, _I, _I]),
+    "lmhead_shard_two_stage": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I, _I, _F,
+                                    _P, _P, _P, _P, _SZ, _P]),
+    "lmhead_shard_softmax": (_I, [_P, _I, _P, _I, _I, _F, _P, _P]),
     "lmhead_draft_select": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "lmhead_verify_chain": (_I, [_P, _I64, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
     "lmhead_cluster_candidate_count": (_I64, [_I64, _I, _I]),

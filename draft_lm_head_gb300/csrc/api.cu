@@ -47,8 +47,12 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t u = 0, tickets = 0, scores = 0, partials = 0, total = 0;
-  int n_tickets = 0;  // ints at `tickets` zeroed by K1: row tickets then tile tickets
+  size_t u = 0, tickets = 0, scores = 0, partials = 0, select = 0, total = 0;
+  // ints at `tickets` zeroed by K1: row tickets, the scoring kernel's tile
+  // tickets, the gather's ready counters (n_ready, 0 when not used), then the
+  // multi-CTA global selection's row states and histograms (at ms_at)
+  int n_tickets = 0, ready_at = 0, n_ready = 0, ms_at = 0;
+  bool ms = false;  // global Top-C through several CTAs per row
 };
 
 bool use_tc(int mode, int r, int T, int k_tile, int M) {
@@ -59,6 +63,30 @@ bool use_tc(int mode, int r, int T, int k_tile, int M) {
 
 bool needs_score_buffer(int mode, int k_tile) {
   return mode == LMHEAD_GLOBAL || k_tile > kFusedMaxKTile;
+}
+
+// The gather waits on per-block ready counters of the fused scoring kernel
+// (instead of its completion) where that kernel publishes them: the dynamic
+// tensor-core kernel (tiles of a multiple of 128 rows) and the GEMV kernel.
+// Measured on the 128256-row head: 2-4 us faster per call at 16-64 hidden
+// vectors, no gain at one, 1.4 us slower at eight, so it is used above eight.
+// LMHEAD_OVERLAP=0 turns it off, =2 uses it at every M (measurements only).
+constexpr int kOverlapMinM = 9;
+int overlap_setting() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("LMHEAD_OVERLAP");
+    v = e ? atoi(e) : 1;
+  }
+  return v;
+}
+
+bool gather_overlaps(int mode, int r, int T, int k_tile, int M) {
+  const int ov = overlap_setting();
+  if (ov == 0 || (ov == 1 && M < kOverlapMinM)) return false;
+  if (mode != LMHEAD_LOCAL || needs_score_buffer(mode, k_tile)) return false;
+  if (use_tc(mode, r, T, k_tile, M)) return T % 128 == 0;
+  return local_topk_gemv_supported(M, r, T, k_tile);
 }
 
 // Columns per block of the warp gather's candidate order in local mode (a
@@ -79,8 +107,17 @@ Layout layout_for(int mode, int64_t n, int d, int r, int M, int C_or_tile, int k
   off = round_up(off + (size_t)M * r * sizeof(bf16_t), 256);
   L.tickets = off;
   const bool tc = use_tc(mode, r, C_or_tile, k_tile, M);
-  L.n_tickets = M + (tc ? local_topk_tc_tickets(n, M, C_or_tile) : 0);
+  L.ready_at = M + (tc ? local_topk_tc_tickets(n, M, C_or_tile) : 0);
+  L.n_ready = gather_overlaps(mode, r, C_or_tile, k_tile, M)
+                  ? ready_words((n + C_or_tile - 1) / C_or_tile) : 0;
+  L.ms = mode == LMHEAD_GLOBAL && row_select_multi(n, M, C_or_tile);
+  L.ms_at = (int)round_up((size_t)(L.ready_at + L.n_ready), 4);  // 16-byte aligned
+  L.n_tickets = L.ms ? L.ms_at + row_select_multi_ints(M) : L.ready_at + L.n_ready;
   off = round_up(off + (size_t)L.n_tickets * sizeof(int), 256);
+  if (L.ms) {
+    L.select = off;
+    off = round_up(off + row_select_multi_bytes(M, C_or_tile), 256);
+  }
   if (tc) {
     L.partials = off;
     off = round_up(off + local_topk_tc_scratch_bytes(n, M, C_or_tile), 256);
@@ -145,26 +182,28 @@ struct Marks {
 };
 
 // Stage 1 on validated arguments; u lives in the workspace.
+// ready: the gather's counters when it overlaps the scoring kernel, else nullptr.
 int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
                const int32_t* token_ids, int64_t n, int d, int r, int M, int C_or_tile,
                int k_tile, int32_t* out_ids, float* out_scores, char* ws, const Layout& L,
-               bool zero_tickets, Marks& mk, cudaStream_t s) {
+               bool zero_tickets, Marks& mk, cudaStream_t s, int* ready = nullptr) {
   bf16_t* u = reinterpret_cast<bf16_t*>(ws + L.u);
   int* tickets = reinterpret_cast<int*>(ws + L.tickets);
   if (mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   const bool tc = use_tc(mode, r, C_or_tile, k_tile, M);
-  const bool zero = zero_tickets || tc;
+  const bool zero = zero_tickets || tc || ready || L.ms;
   cudaError_t e = launch_project_u(B, h, d, r, M, u, zero ? tickets : nullptr,
                                    zero ? L.n_tickets : 0, s);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   if (tc) {
     e = launch_local_topk_tc(A, u, token_ids, n, r, M, C_or_tile, k_tile, out_ids, out_scores,
-                             ws + L.partials, tickets + M, device_error_word(), s);
+                             ws + L.partials, tickets + M, device_error_word(), s, ready);
     if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
     return LMHEAD_OK;
   }
   if (!needs_score_buffer(mode, k_tile)) {
-    e = launch_local_topk_fma(A, u, token_ids, n, r, M, C_or_tile, k_tile, out_ids, out_scores, s);
+    e = launch_local_topk_fma(A, u, token_ids, n, r, M, C_or_tile, k_tile, out_ids, out_scores, s,
+                              ready);
     if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
     return LMHEAD_OK;
   }
@@ -173,7 +212,12 @@ int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   const int64_t seg = mode == LMHEAD_GLOBAL ? n : C_or_tile;
   const int k = mode == LMHEAD_GLOBAL ? C_or_tile : k_tile;
-  e = launch_segment_topk(S, token_ids, n, M, seg, k, out_ids, out_scores, device_error_word(), s);
+  if (L.ms)
+    e = launch_row_select_multi(S, token_ids, n, M, k, out_ids, out_scores, tickets + L.ms_at,
+                                ws + L.select, s);
+  else
+    e = launch_segment_topk(S, token_ids, n, M, seg, k, out_ids, out_scores, device_error_word(),
+                            s);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   return LMHEAD_OK;
 }
@@ -212,6 +256,9 @@ ClusterLayout cluster_layout(int64_t n, int d, int r, int M, int group) {
   return C;
 }
 
+// Stages of a call (each one timing mark): projection, scoring, selection
+// when the mode needs one (the multi-CTA global selection launches seven
+// kernels inside its stage), gather, softmax.
 int launches_for(int mode, int k_tile) { return needs_score_buffer(mode, k_tile) ? 5 : 4; }
 
 bool valid_temperature(float t) { return t > 0.f && isfinite(t); }
@@ -319,14 +366,18 @@ static int two_stage_impl(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
     return LMHEAD_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = (cudaStream_t)stream;
+  int* ready = L.n_ready ? reinterpret_cast<int*>(ws + L.tickets) + L.ready_at : nullptr;
   st = run_select(mode, A, B, h, token_ids, n, d, r, M, C_or_tile, k_tile, out_ids, nullptr, ws,
-                  L, true, mk, s);
+                  L, true, mk, s, ready);
   if (st != LMHEAD_OK) return st;
   const int K = (int)candidate_count(mode, n, C_or_tile, k_tile);
-  // stage 2: exact logits of the candidates, then their softmax (one CTA per row)
+  // stage 2: exact logits of the candidates (block by block as the scoring
+  // kernel finishes them, when it publishes ready counters), then their
+  // softmax (one CTA per row)
   cudaError_t e = launch_gather_logits(W, h, out_ids, n, d, M, K, out_logits, nullptr, 1.f,
                                        nullptr, device_error_word(), s,
-                                       mode == LMHEAD_LOCAL ? gather_span(k_tile) : 0);
+                                       mode == LMHEAD_LOCAL ? gather_span(k_tile) : 0, ready,
+                                       k_tile, (n + C_or_tile - 1) / C_or_tile);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   e = launch_row_softmax(out_logits, M, K, 1.f / temperature, out_q, s);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
@@ -453,6 +504,56 @@ int lmhead_cluster_two_stage(const lmhead_bf16* W, const lmhead_bf16* A, const l
                              device_error_word(), s, 0);
   if (e == cudaSuccess) e = launch_row_softmax(out_logits, M, K, 1.f / temperature, out_q, s);
   return cuda_status(e);
+}
+
+size_t lmhead_shard_workspace_size(int64_t n_shard, int d, int r, int M, int T, int k_tile) {
+  return lmhead_workspace_size(LMHEAD_LOCAL, n_shard, d, r, M, T, k_tile);
+}
+
+int lmhead_shard_two_stage(const lmhead_bf16* W_shard, const lmhead_bf16* A_shard,
+                           const lmhead_bf16* B, const lmhead_bf16* h,
+                           const int32_t* token_ids_shard, const int32_t* row_of_id,
+                           int64_t n_vocab, int64_t n_shard, int d, int r, int M, int T,
+                           int k_tile, float temperature, int32_t* out_ids, float* out_logits,
+                           float* out_stats, void* workspace, size_t workspace_bytes,
+                           lmhead_stream stream) {
+  if (!W_shard || !A_shard || !B || !h || !token_ids_shard || !row_of_id || !out_ids ||
+      !out_logits || !out_stats)
+    return LMHEAD_ERR_NULL;
+  if (n_vocab < 1 || n_vocab > INT32_MAX || n_shard > n_vocab) return LMHEAD_ERR_SHAPE;
+  int st = check_select(LMHEAD_LOCAL, n_shard, d, r, M, T, k_tile);
+  if (st != LMHEAD_OK) return st;
+  if (!valid_temperature(temperature)) return LMHEAD_ERR_SHAPE;
+  if (!aligned16(W_shard) || !aligned16(A_shard) || !aligned16(B) || !aligned16(h) ||
+      !aligned16(token_ids_shard) || !aligned16(out_ids))
+    return LMHEAD_ERR_ALIGN;
+  const Layout L = layout_for(LMHEAD_LOCAL, n_shard, d, r, M, T, k_tile);
+  if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return LMHEAD_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = (cudaStream_t)stream;
+  int* ready = L.n_ready ? reinterpret_cast<int*>(ws + L.tickets) + L.ready_at : nullptr;
+  Marks none;
+  // stage 1 over the shard's positions; ids come out in vocabulary space
+  st = run_select(LMHEAD_LOCAL, A_shard, B, h, token_ids_shard, n_shard, d, r, M, T, k_tile,
+                  out_ids, nullptr, ws, L, true, none, s, ready);
+  if (st != LMHEAD_OK) return st;
+  const int K = (int)candidate_count(LMHEAD_LOCAL, n_shard, T, k_tile);
+  // stage 2 on the shard's own rows of W (row_of_id: vocabulary id -> local row)
+  cudaError_t e = launch_gather_logits(W_shard, h, out_ids, n_vocab, d, M, K, out_logits, nullptr,
+                                       1.f, nullptr, device_error_word(), s, gather_span(k_tile),
+                                       ready, k_tile, (n_shard + T - 1) / T, row_of_id, n_shard);
+  if (e == cudaSuccess) e = launch_row_stats(out_logits, M, K, 1.f / temperature, out_stats, s);
+  return cuda_status(e);
+}
+
+int lmhead_shard_softmax(const float* all_stats, int G, const float* logits, int M, int K,
+                         float temperature, float* out_q, lmhead_stream stream) {
+  if (!all_stats || !logits || !out_q) return LMHEAD_ERR_NULL;
+  if (G < 1 || G > 65536 || M < 1 || K < 1 || M > 2147483647 / K) return LMHEAD_ERR_SHAPE;
+  if (!valid_temperature(temperature)) return LMHEAD_ERR_SHAPE;
+  return cuda_status(launch_shard_softmax(all_stats, G, logits, M, K, 1.f / temperature, out_q,
+                                          (cudaStream_t)stream));
 }
 
 int64_t lmhead_debug_set_wait_cycles(int64_t cycles) {

@@ -136,6 +136,41 @@ __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// ---- ready counters between the scoring kernel and the gather
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// A bounded wait on another kernel's progress gives up after this many SM
+// clock cycles (about a second).
+constexpr long long kCounterWaitCycles = 2000000000ll;
+
+// Wait until *counter >= need. Gives up (false) when *stop is set (the
+// producing kernel aborted on a timeout of its own) or after
+// kCounterWaitCycles (then records a timeout in `err`).
+__device__ __forceinline__ bool wait_count(const int* counter, int need, const int* stop,
+                                           int* err) {
+  const long long t0 = clock64();
+  while (ld_acquire(counter) < need) {
+    if (*reinterpret_cast<const volatile int*>(stop) != 0) return false;
+    if (clock64() - t0 > kCounterWaitCycles) {
+      record_error(err, kDevErrTimeout);
+      return false;
+    }
+    __nanosleep(256);
+  }
+  return true;
+}
+
+// Publish `count` more ready rows on `counter`, after this thread's and (by
+// a preceding CTA barrier) its CTA's earlier stores.
+__device__ __forceinline__ void signal_count(int* counter, int count) {
+  __threadfence();
+  atomicAdd(counter, count);
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -80,7 +80,9 @@ __global__ void __launch_bounds__(WPC * 32, MINB)
 gather_logits_kernel(const bf16_t* __restrict__ W, const bf16_t* __restrict__ h,
                      const int32_t* __restrict__ ids, int64_t n, int d, int M, int K,
                      int span, float* __restrict__ logits, float* __restrict__ q,
-                     float inv_temp, int* __restrict__ tickets, int* __restrict__ err) {
+                     float inv_temp, int* __restrict__ tickets, int* __restrict__ err,
+                     const int* __restrict__ ready, int k_tile, int tiles,
+                     const int32_t* __restrict__ row_of_id, int64_t n_rows) {
   extern __shared__ uint4 h_s[];
   const int lane = threadIdx.x & 31;
   const uint32_t MK = (uint32_t)M * (uint32_t)K;
@@ -101,17 +103,34 @@ gather_logits_kernel(const bf16_t* __restrict__ W, const bf16_t* __restrict__ h,
       cta_sync();
     }
   }
-  pdl_wait();  // ids come from the previous kernel
+  // ids come from the previous kernel: wait for all of it, or (ready) only
+  // for the block of tiles that holds this warp's candidate
+  if (!ready) pdl_wait();
   if (c >= MK) return;
   int m;
   const uint32_t flat = candidate_of(c, M, K, span, &m);
-  const int32_t id = __ldg(ids + flat);
+  if (ready) {
+    if (lane == 0) {
+      const int b = (int)((flat - (uint32_t)m * (uint32_t)K) / (uint32_t)k_tile) / kReadyTiles;
+      wait_count(ready + b, min(kReadyTiles, tiles - b * kReadyTiles) * M,
+                 ready + ready_blocks(tiles), err);
+    }
+    __syncwarp();
+  }
+  const int32_t id = __ldcg(ids + flat);
+  // the W row of the id: the id itself, or (a vocabulary shard) its local row
+  int64_t row = id;
+  bool bad = id < 0 || (int64_t)id >= n;
+  if (!bad && row_of_id) {
+    row = __ldg(row_of_id + id);
+    bad = row < 0 || row >= n_rows;
+  }
   float s;
-  if (id < 0 || (int64_t)id >= n) {
+  if (bad) {
     if (lane == 0) record_error(err, kDevErrBadId);
     s = __int_as_float(0x7FC00000);  // NaN
   } else {
-    const uint4* wrow = reinterpret_cast<const uint4*>(W + (size_t)id * d);
+    const uint4* wrow = reinterpret_cast<const uint4*>(W + (size_t)row * d);
     const uint4* hrow = reinterpret_cast<const uint4*>(h + (size_t)m * d);
     float acc = 0.f;
     if (staged) {
@@ -289,7 +308,8 @@ row_softmax_reg_kernel(const float* __restrict__ L, int K, float inv_temp, float
 template <int WPC, int UNR, int MINB, bool SH>
 cudaError_t launch_gather_v(const bf16_t* W, const bf16_t* h, const int32_t* ids, int64_t n, int d,
                             int M, int K, float* logits, float* q, float inv_temp, int* tickets,
-                            int* err, cudaStream_t s, int span) {
+                            int* err, cudaStream_t s, int span, const int* ready, int k_tile,
+                            int64_t tiles, const int32_t* row_of_id, int64_t n_rows) {
   const int64_t total = (int64_t)M * K;
   const unsigned grid = (unsigned)((total + WPC - 1) / WPC);
   const size_t smem = SH ? (size_t)d * 2 : 0;
@@ -300,14 +320,18 @@ cudaError_t launch_gather_v(const bf16_t* W, const bf16_t* h, const int32_t* ids
   }
   return launch_kernel(true, gather_logits_kernel<WPC, UNR, MINB, SH>, dim3(grid),
                        dim3(WPC * 32), smem, s, W, h, ids, n, d, M, K, span, logits, q,
-                       inv_temp, tickets, err);
+                       inv_temp, tickets, err, ready, k_tile, (int)tiles, row_of_id, n_rows);
 }
 
 cudaError_t launch_gather_logits(const bf16_t* W, const bf16_t* h, const int32_t* ids, int64_t n,
                                  int d, int M, int K, float* logits, float* q, float inv_temp,
-                                 int* tickets, int* err, cudaStream_t s, int span) {
+                                 int* tickets, int* err, cudaStream_t s, int span,
+                                 const int* ready, int k_tile, int64_t tiles,
+                                 const int32_t* row_of_id, int64_t n_rows) {
+  if (ready && (k_tile < 1 || tiles < 1)) return cudaErrorInvalidValue;
   return launch_gather_v<kWarpsPerCta, 4, 6, true>(W, h, ids, n, d, M, K, logits, q, inv_temp,
-                                                     tickets, err, s, span);
+                                                     tickets, err, s, span, ready, k_tile, tiles,
+                                                     row_of_id, n_rows);
 }
 
 cudaError_t launch_row_softmax(const float* L, int M, int64_t K, float inv_temp, float* q,

@@ -27,9 +27,10 @@ cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int
 // r = 256) it runs the warp-per-row GEMV kernel.
 constexpr int kLocalGemvMaxM = 2;
 bool local_topk_gemv_supported(int M, int r, int T, int k_tile);
+// ready: the gather's ready counters (GEMV kernel only; may be nullptr).
 cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
                                   int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,
-                                  float* out_scores, cudaStream_t s);
+                                  float* out_scores, cudaStream_t s, int* ready = nullptr);
 
 // K4 (tensor cores): tcgen05 MMA with TMA-staged A chunks, persistent CTAs.
 constexpr int kLocalTcMaxR = 512;
@@ -38,10 +39,12 @@ bool local_topk_tc_supported(int r, int T, int k_tile);
 // workspace bytes for the split-tile partial lists; tile tickets are counted separately
 size_t local_topk_tc_scratch_bytes(int64_t n, int M, int T);
 int local_topk_tc_tickets(int64_t n, int M, int T);
+// ready: the gather's ready counters (tiles of a multiple of 128 rows only;
+// may be nullptr).
 cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
                                  int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,
                                  float* out_scores, void* partials, int* tile_tickets, int* err,
-                                 cudaStream_t s);
+                                 cudaStream_t s, int* ready = nullptr);
 
 // K3: per row m, per segment of `seg_len` positions, exact top-k of S by
 // (score desc, vocabulary id asc). k <= kSelectMaxK.
@@ -49,13 +52,53 @@ cudaError_t launch_segment_topk(const float* S, const int32_t* token_ids, int64_
                                 int64_t seg_len, int k, int32_t* out_ids, float* out_scores,
                                 int* err, cudaStream_t s);
 
+// Overlap of the gather with the fused scoring kernel (local mode): the
+// scoring kernel counts, per block of kReadyTiles consecutive tiles, the
+// hidden rows whose ids of the block's tiles it has written (ready[b] reaches
+// tiles_in_block * M when block b is complete); the gather waits on those
+// counters instead of on the scoring kernel's completion. The counters, and
+// after them one stop word that the scoring kernel sets if it aborts, live in
+// the workspace's ticket area, zeroed by the projection kernel every call.
+constexpr int kReadyTiles = 16;
+__host__ __device__ inline int ready_blocks(int64_t tiles) {
+  return (int)((tiles + kReadyTiles - 1) / kReadyTiles);
+}
+inline int ready_words(int64_t tiles) { return ready_blocks(tiles) + 1; }  // counters + stop
+
+// K3 for long rows and few of them (global Top-k, several CTAs per row):
+// `zero` holds row_select_multi_ints(M) ints that are zero on entry (the
+// projection kernel zeroes them), `scratch` row_select_multi_bytes(M, k)
+// bytes (no initial value). Same result and order as launch_segment_topk with
+// one segment per row.
+bool row_select_multi(int64_t n, int M, int k);
+int row_select_multi_ints(int M);
+size_t row_select_multi_bytes(int M, int k);
+cudaError_t launch_row_select_multi(const float* S, const int32_t* token_ids, int64_t n, int M,
+                                    int k, int32_t* out_ids, float* out_scores, int* zero,
+                                    void* scratch, cudaStream_t s);
+
 // K5 (+K6 fused when q != nullptr): L[m,j] = W[ids[m,j]] . h[m]; q = softmax.
 // `tickets` (M ints, zero on entry, left zero on exit) enable the fusion.
 // span > 0: warps take the candidates in blocks of `span` columns (all rows
 // of a block together) instead of row by row; see the kernel.
+// ready != nullptr: wait on the scoring kernel's ready counters (tiles of
+// k_tile columns, `tiles` in all) instead of on its completion.
+// row_of_id != nullptr: W holds n_rows rows, the row of vocabulary id i being
+// row_of_id[i] (a vocabulary shard; ids outside it are bad ids).
 cudaError_t launch_gather_logits(const bf16_t* W, const bf16_t* h, const int32_t* ids, int64_t n,
                                  int d, int M, int K, float* logits, float* q, float inv_temp,
-                                 int* tickets, int* err, cudaStream_t s, int span = 0);
+                                 int* tickets, int* err, cudaStream_t s, int span = 0,
+                                 const int* ready = nullptr, int k_tile = 0, int64_t tiles = 0,
+                                 const int32_t* row_of_id = nullptr, int64_t n_rows = 0);
+
+// Vocabulary shards: per row of L (M x K), stats[m] = (max_j L/T, sum_j
+// exp(L/T - max)); and q of one shard's candidates from all G shards' stats
+// (G x M x 2, any order): q = exp(L/T - Mx) / Z, Mx = max of the maxima,
+// Z = sum_g sum_g exp(max_g - Mx).
+cudaError_t launch_row_stats(const float* L, int M, int K, float inv_temp, float* stats,
+                             cudaStream_t s);
+cudaError_t launch_shard_softmax(const float* all_stats, int G, const float* L, int M, int K,
+                                 float inv_temp, float* q, cudaStream_t s);
 
 // K6 standalone: row softmax of an M x K matrix (any K).
 cudaError_t launch_row_softmax(const float* L, int M, int64_t K, float inv_temp, float* q,

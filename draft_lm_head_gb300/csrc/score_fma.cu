@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kGemvThreads, DB ? (MB == 1 ? 3 : 2) : (MB == 
 local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u,
                        const int32_t* __restrict__ token_ids, int64_t n, int r, int M, int T,
                        int k_tile, int K, int32_t* __restrict__ out_ids,
-                       float* __restrict__ out_scores) {
+                       float* __restrict__ out_scores, int* __restrict__ ready) {
   __shared__ float sc[MB][kGemvThreads];
   __shared__ int32_t svid[kGemvThreads];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -208,6 +208,9 @@ local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ 
   };
   load_batch(0);  // A before waiting for u
   pdl_wait();     // u is written by the previous kernel
+  // the gather may launch once every thread has triggered, which is after
+  // the projection kernel (that zeroes the ready counters) completed
+  pdl_trigger();
   float uf[MB][8];
 #pragma unroll
   for (int mm = 0; mm < MB; ++mm) {
@@ -295,16 +298,25 @@ local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ 
       }
     }
   }
+  if (ready) {  // this CTA's tiles (one ready block: 256 / T divides 16) are written
+    __threadfence();
+    cta_sync();
+    if (tid == 0) {
+      const int64_t tile0 = (int64_t)blockIdx.x * tpc;
+      const int64_t tiles_here = min((int64_t)tpc, (n + T - 1) / T - tile0);
+      signal_count(ready + tile0 / kReadyTiles, (int)tiles_here * mb);
+    }
+  }
 }
 
 template <int MB, bool DB>
 cudaError_t launch_gemv_mb(const bf16_t* A, const bf16_t* u, const int32_t* token_ids, int64_t n,
                            int r, int M, int T, int k_tile, int K, int32_t* out_ids,
-                           float* out_scores, cudaStream_t s) {
+                           float* out_scores, cudaStream_t s, int* ready) {
   dim3 grid((unsigned)((n + kGemvThreads - 1) / kGemvThreads), (unsigned)((M + MB - 1) / MB));
 #define GV(KT)                                                                                \
   return launch_kernel(true, local_topk_gemv_kernel<MB, KT, DB>, grid, dim3(kGemvThreads), 0, s, \
-                       A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores);
+                       A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, ready);
   if (k_tile <= 1) GV(1);
   if (k_tile <= 2) GV(2);
   if (k_tile <= 4) GV(4);
@@ -331,7 +343,7 @@ bool local_topk_gemv_supported(int M, int r, int T, int k_tile) {
 
 cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
                                   int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,
-                                  float* out_scores, cudaStream_t s) {
+                                  float* out_scores, cudaStream_t s, int* ready) {
   const int64_t tiles = (n + T - 1) / T;
   const int64_t full = n / T, tail = n - full * T;
   const int K = (int)(full * k_tile + (tail ? (tail < k_tile ? tail : k_tile) : 0));
@@ -339,8 +351,10 @@ cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_
     // measured: one hidden vector, four CTAs per SM (all 501 CTAs of the
     // 128256-row head resident at once); two, the next rows requested early
     if (M <= 1)
-      return launch_gemv_mb<1, false>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s);
-    return launch_gemv_mb<2, true>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s);
+      return launch_gemv_mb<1, false>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores,
+                                      s, ready);
+    return launch_gemv_mb<2, true>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s,
+                                   ready);
   }
   // the kernel also has ~13 KB of static shared memory, so the opt-in is
   // needed below 48 KB of dynamic memory too: always raise the limit (cached)

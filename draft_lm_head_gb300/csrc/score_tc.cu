@@ -77,6 +77,7 @@ struct Params {
   int* tile_tickets;  // [HC][tiles]
   int* err;
   long long wait_cycles;  // budget of every role wait (drains keep tc::kWaitCycles)
+  int* ready;             // dynamic kernel: the gather's ready counters, or nullptr
 };
 
 __device__ __forceinline__ int32_t vocab_id(const Params& p, int64_t pos) {
@@ -622,6 +623,7 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
       // u is written by the previous kernel: wait for it, then load it once
       auto load_u = [&]() {
         pdl_wait();
+        pdl_trigger();  // the projection is done (see the epilogue)
         tc::mbar_arrive_expect_tx(&ctl.ufull, (uint32_t)(kblocks * kStageBytes));
         for (int ub = 0; ub < kblocks; ++ub)
           for (int rep = 0; rep < p.R; ++rep)
@@ -693,7 +695,6 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
         *abort_flag = 1;
         record_error(p.err, kDevErrTimeout);
       }
-      pdl_trigger();
       if (*abort_flag) {
         const uint32_t first = it > (uint32_t)NS ? it - NS : 0;
         for (uint32_t jq = first; jq < it; ++jq) {
@@ -706,11 +707,18 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
         while (u_loaded && !tc::mbar_try_wait(&ctl.ufull, 0) && clock64() - t0 < tc::kWaitCycles) {
         }
       }
+    } else {
+      pdl_wait();
+      pdl_trigger();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = tc::mbar_wait(&ctl.ufull, 0, abort_flag, p.wait_cycles);
+      if (ok) {
+        pdl_wait();  // returns at once: u is loaded, so the projection is done
+        pdl_trigger();
+      }
       uint32_t it = 0;
       for (int c = 0; ok; ++c) {
         const int a = c % kNAcc;
@@ -745,10 +753,18 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
         record_error(p.err, kDevErrTimeout);
         tc::mma_drain(&ctl.mma_drain);  // TMEM is freed below
       }
+    } else {
+      pdl_wait();
+      pdl_trigger();
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // The gather that follows may launch once every thread of every CTA has
+    // triggered; each thread triggers only after the projection kernel has
+    // completed, so the gather never sees the ready counters before the
+    // projection kernel zeroed them.
     pdl_wait();
+    pdl_trigger();
     const int q = warp & 3;
     const int ml = q * 32 + lane;
     const int rep = (q * 32) / p.rows_per_rep;
@@ -757,6 +773,9 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
     const bool valid_out = valid && rep == 0;
     const int m_lo = y * p.rows_per_rep + (q * 32) % p.rows_per_rep - p.lane_shift;
     const bool warp_live = m_lo + 31 >= 0 && m_lo < p.M;
+    // hidden rows of this chunk (what one finished tile adds to its ready count)
+    const int rows_valid = max(0, min(p.M, (y + 1) * p.rows_per_rep - p.lane_shift) -
+                                      max(0, y * p.rows_per_rep - p.lane_shift));
     const float kNaN = __int_as_float(0x7FC00000);
     const int cols = CH / p.R;
     const int jb = rep * cols;
@@ -833,6 +852,11 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
         if (valid_out)
           write_tile<KT>(p, m, tile, (int)min((int64_t)KT, min(n, (int64_t)(tile + 1) * T) - (int64_t)tile * T),
                          Lst, true);
+        if (p.ready) {  // this tile's ids of this chunk's hidden rows are written
+          __threadfence();
+          named_sync(2, 128);
+          if (warp == 2 && lane == 0) signal_count(p.ready + tile / kReadyTiles, rows_valid);
+        }
 #pragma unroll
         for (int jj = 0; jj < kSub; ++jj) sub[jj].reset();
       }
@@ -845,6 +869,9 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+  // an aborted CTA will not publish its tiles: release the gather's waits
+  if (p.ready && threadIdx.x == 0 && *abort_flag)
+    atomicExch(p.ready + ready_blocks(p.tiles), 1);
 }
 
 // ---------------------------------------------------------------- host side
@@ -904,7 +931,7 @@ int local_topk_tc_tickets(int64_t n, int M, int T) {
 cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
                                  int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,
                                  float* out_scores, void* partials, int* tile_tickets, int* err,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, int* ready) {
   Params p;
   p.token_ids = token_ids;
   p.n = n;
@@ -941,6 +968,7 @@ cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t
   p.tile_tickets = tile_tickets;
   p.err = err;
   p.wait_cycles = role_wait_cycles();
+  p.ready = (T % kChunk == 0) ? ready : nullptr;  // only the dynamic kernel signals
   CUtensorMap amap, umap;
   if (!make_bf16_map(&amap, A, (uint64_t)n, (uint64_t)r, ch, kKBlock) ||
       !make_bf16_map(&umap, u, (uint64_t)M, (uint64_t)r, p.rows_per_rep, kKBlock))

@@ -165,7 +165,197 @@ segment_topk_kernel(const float* __restrict__ S, const int32_t* __restrict__ tok
   }
 }
 
+// ---------------------------------------------------------------- long rows, few rows
+// Global Top-k of rows too long for one CTA to sweep quickly (one CTA per row
+// does every radix pass over the whole row: ~100 us at n = 128256). Here G
+// CTAs share a row. Pass kernels (up to six launches, 12-bit digits from the
+// top of the key): each CTA histograms the keys of its segment that lie in
+// the row's current range [lo, hi] and adds the histogram into the row's
+// global one; the last CTA of the row to finish (atomic ticket, no waiting)
+// finds the boundary digit, narrows [lo, hi], counts the keys above it and
+// marks the row done once the range holds at most kCap keys. Later passes of
+// a done row return at once. Collection kernel: every CTA appends its keys
+// above the range and inside it to two per-row lists; the last CTA sorts the
+// survivors (at most k + kCap keys) and writes the row's Top-k, score
+// descending, ties by the smaller vocabulary id (the keys are unique).
+constexpr int kMsThreads = 1024;
+constexpr int kMsPasses = 6;      // 64-bit keys, 12-bit digits (the last ones overlap)
+constexpr int kMsStateInts = 16;  // per-row state, then the row's kBins histogram
+
+struct MsState {
+  unsigned long long lo, hi;  // current key range (meaningful once pass > 0)
+  int gt;                     // keys above hi
+  int done;                   // the range holds <= kCap keys
+  int ticket;                 // CTAs of the row finished with the current kernel
+  int pass;                   // passes completed
+  int n_sel, n_cand;          // collection counters
+};
+static_assert(sizeof(MsState) <= kMsStateInts * sizeof(int), "state slot");
+
+__device__ __forceinline__ int64_t ms_seg(int64_t n, int G) { return (n + G - 1) / G; }
+
+// grid (G, M). `zero`: M x (kMsStateInts + kBins) ints, zero before the
+// first pass of a call.
+__global__ void __launch_bounds__(kMsThreads)
+ms_pass_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_ids, int64_t n,
+               int k, int* __restrict__ zero) {
+  __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t part[kMsThreads];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, G = gridDim.x, m = blockIdx.y;
+  int* zr = zero + (size_t)m * (kMsStateInts + kBins);
+  MsState* st = reinterpret_cast<MsState*>(zr);
+  uint32_t* ghist = reinterpret_cast<uint32_t*>(zr + kMsStateInts);
+  pdl_wait();  // scores, and the state the previous pass left
+  pdl_trigger();
+  if (*reinterpret_cast<volatile int*>(&st->done)) return;
+  const int pass = st->pass;
+  const uint64_t lo = pass ? st->lo : 0ull, hi = pass ? st->hi : ~0ull;
+  const int gt = st->gt;
+  const int shift = max(0, 64 - kDigit * (pass + 1));
+  const int64_t per = ms_seg(n, G);
+  const int64_t p0 = (int64_t)blockIdx.x * per, p1 = min(n, p0 + per);
+  const float* row = S + (size_t)m * n;
+  for (int i = tid; i < kBins; i += kMsThreads) hist[i] = 0;
+  cta_sync();
+  for (int64_t p = p0 + tid; p < p1; p += kMsThreads) {
+    const uint64_t key = key_at(row, token_ids, p);
+    if (key >= lo && key <= hi) atomicAdd(&hist[(key >> shift) & (kBins - 1)], 1u);
+  }
+  cta_sync();
+  for (int i = tid; i < kBins; i += kMsThreads)
+    if (hist[i]) atomicAdd(&ghist[i], hist[i]);
+  __threadfence();
+  cta_sync();
+  if (tid == 0) s_last = atomicAdd(&st->ticket, 1) == G - 1;
+  cta_sync();
+  if (!s_last) return;
+  // the last CTA of the row: the row's histogram is complete
+  __threadfence();
+  for (int i = tid; i < kBins; i += kMsThreads) {
+    hist[i] = __ldcg(ghist + i);
+    ghist[i] = 0;  // ready for the next pass
+  }
+  cta_sync();
+  const int g = kMsThreads - 1 - tid;  // thread tid owns bins [4g, 4g+4), descending order
+  const uint32_t local = hist[4 * g] + hist[4 * g + 1] + hist[4 * g + 2] + hist[4 * g + 3];
+  part[tid] = local;
+  cta_sync();
+  for (int off = 1; off < kMsThreads; off <<= 1) {
+    const uint32_t v = tid >= off ? part[tid - off] : 0u;
+    cta_sync();
+    part[tid] += v;
+    cta_sync();
+  }
+  uint32_t above = part[tid] - local;
+  const uint32_t need = (uint32_t)(min((int64_t)k, n) - gt);
+  if (above < need && above + local >= need) {
+    for (int b = 4 * g + 3; b >= 4 * g; --b) {
+      if (above + hist[b] >= need) {
+        const uint64_t prefix =
+            lo & ~((((uint64_t)kBins - 1) << shift) | ((1ull << shift) - 1ull));
+        const uint64_t nlo = prefix | ((uint64_t)b << shift);
+        st->lo = nlo;
+        st->hi = nlo | ((1ull << shift) - 1ull);
+        st->gt = gt + (int)above;
+        st->done = (hist[b] <= (uint32_t)kCap || shift == 0) ? 1 : 0;
+        break;
+      }
+      above += hist[b];
+    }
+  }
+  if (tid == 0) {
+    st->pass = pass + 1;
+    st->ticket = 0;
+  }
+}
+
+// grid (G, M); dynamic shared memory: the last CTA's sort buffer.
+__global__ void __launch_bounds__(kMsThreads)
+ms_collect_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_ids, int64_t n,
+                  int k, int* __restrict__ zero, uint64_t* __restrict__ sel,
+                  uint64_t* __restrict__ cand, int32_t* __restrict__ out_ids,
+                  float* __restrict__ out_scores) {
+  extern __shared__ uint64_t keys[];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, G = gridDim.x, m = blockIdx.y;
+  MsState* st = reinterpret_cast<MsState*>(zero + (size_t)m * (kMsStateInts + kBins));
+  pdl_wait();
+  pdl_trigger();
+  const uint64_t lo = st->lo, hi = st->hi;
+  const int kk = (int)min((int64_t)k, n);
+  uint64_t* rsel = sel + (size_t)m * k;
+  uint64_t* rcand = cand + (size_t)m * kCap;
+  const int64_t per = ms_seg(n, G);
+  const int64_t p0 = (int64_t)blockIdx.x * per, p1 = min(n, p0 + per);
+  const float* row = S + (size_t)m * n;
+  for (int64_t p = p0 + tid; p < p1; p += kMsThreads) {
+    const uint64_t key = key_at(row, token_ids, p);
+    if (key > hi) {
+      const int i = atomicAdd(&st->n_sel, 1);
+      if (i < kk) rsel[i] = key;
+    } else if (key >= lo) {
+      const int i = atomicAdd(&st->n_cand, 1);
+      if (i < kCap) rcand[i] = key;
+    }
+  }
+  __threadfence();
+  cta_sync();
+  if (tid == 0) s_last = atomicAdd(&st->ticket, 1) == G - 1;
+  cta_sync();
+  if (!s_last) return;
+  __threadfence();
+  const int ns = min(__ldcg(&st->n_sel), kk), nc = min(__ldcg(&st->n_cand), kCap);
+  const int P = pow2_at_least(ns + nc);
+  for (int i = tid; i < P; i += kMsThreads)
+    keys[i] = i < ns ? __ldcg(rsel + i) : (i < ns + nc ? __ldcg(rcand + i - ns) : 0ull);
+  cta_sync();
+  bitonic_desc(keys, P);
+  const int take = min(kk, ns + nc);
+  for (int j = tid; j < take; j += kMsThreads) {
+    out_ids[(size_t)m * k + j] = key_id(keys[j]);
+    if (out_scores) out_scores[(size_t)m * k + j] = key_score(keys[j]);
+  }
+}
+
+int ms_ctas(int64_t n, int M, int sms) {
+  const int64_t want = (4 * (int64_t)sms + M - 1) / M;
+  const int64_t cap = (n + 2047) / 2048;  // at least ~2 keys per thread
+  return (int)max((int64_t)1, min(want, cap));
+}
+
 }  // namespace
+
+bool row_select_multi(int64_t n, int M, int k) {
+  return n > 2 * kCap && k <= kCap && M <= 2 * 152;
+}
+
+int row_select_multi_ints(int M) { return M * (kMsStateInts + kBins); }
+
+size_t row_select_multi_bytes(int M, int k) {
+  return (size_t)M * ((size_t)k + kCap) * sizeof(uint64_t);
+}
+
+cudaError_t launch_row_select_multi(const float* S, const int32_t* token_ids, int64_t n, int M,
+                                    int k, int32_t* out_ids, float* out_scores, int* zero,
+                                    void* scratch, cudaStream_t s) {
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const dim3 grid((unsigned)ms_ctas(n, M, sms), (unsigned)M);
+  for (int pass = 0; pass < kMsPasses; ++pass) {
+    cudaError_t e = launch_kernel(true, ms_pass_kernel, grid, dim3(kMsThreads), 0, s, S, token_ids,
+                                  n, k, zero);
+    if (e != cudaSuccess) return e;
+  }
+  uint64_t* sel = static_cast<uint64_t*>(scratch);
+  uint64_t* cand = sel + (size_t)M * k;
+  const size_t smem = (size_t)2 * kCap * sizeof(uint64_t);  // k + kCap <= 2 kCap keys
+  static int smem_set[64] = {0};
+  cudaError_t e = ensure_dynamic_smem(ms_collect_kernel, smem, smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(true, ms_collect_kernel, grid, dim3(kMsThreads), smem, s, S, token_ids, n, k,
+                       zero, sel, cand, out_ids, out_scores);
+}
 
 cudaError_t launch_segment_topk(const float* S, const int32_t* token_ids, int64_t n, int M,
                                 int64_t seg_len, int k, int32_t* out_ids, float* out_scores,

@@ -161,9 +161,11 @@ int lmhead_two_stage(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
 
 /*
  * lmhead_two_stage with timing marks for profiling: records events[0] on
- * `stream` before the first kernel and events[i] after the i-th kernel
- * launch, for i < n_events (events are cudaEvent_t created by the caller).
- * lmhead_two_stage_launches gives the number of kernels a call launches.
+ * `stream` before the first kernel and events[i] after the i-th stage, for
+ * i < n_events (events are cudaEvent_t created by the caller). The stages are
+ * the projection, the scoring, the selection (global mode and local k_tile
+ * > 32 only; for long rows it is several kernels), the gather and the
+ * softmax; lmhead_two_stage_launches gives their number.
  * Same arguments, outputs and errors as lmhead_two_stage otherwise.
  */
 int lmhead_two_stage_profiled(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
@@ -313,6 +315,53 @@ int lmhead_verify_chain(const float* p, int64_t n, int B, int Kd, const int32_t*
                         const int32_t* cand_ids, const float* cand_q, int K, const float* r,
                         const float* u, int32_t* out_tokens, int32_t* out_count,
                         lmhead_stream stream);
+
+/*
+ * Vocabulary-sharded local head, one shard of G (one GPU each). The EAGLE-4
+ * notes' local Top-k ("A Local Top-k based variant") picks every tile's
+ * candidates from that tile alone, so when the shuffled positions are split
+ * into contiguous ranges of whole tiles the shards select independently and
+ * the union of their candidates is the unsharded head's. Each shard gathers
+ * its own candidates' rows; only the softmax spans the shards: every shard
+ * reduces its candidates to (max, sum of exponentials) per row, the caller
+ * exchanges those M x 2 floats (an all-gather), and lmhead_shard_softmax
+ * finishes each shard's q. Offline, per shard holding positions [p0, p1):
+ *   A_shard          n_shard x r bf16: rows p0.. of the shuffled A.
+ *   token_ids_shard  n_shard int32: the vocabulary ids of those positions.
+ *   W_shard          n_shard x d bf16: W_shard[i] = W[token_ids_shard[i]].
+ *   row_of_id        n_vocab int32: the local row of each vocabulary id held
+ *                    by this shard, -1 for the others.
+ * B r x d and h M x d are replicated. T, k_tile, temperature as for
+ * lmhead_two_stage in local mode; every shard but the last should hold a
+ * multiple of T positions (otherwise its last tile is short, as at the end
+ * of the head).
+ *   out_ids     M x K_s int32 vocabulary ids (K_s = lmhead_candidate_count(
+ *               LMHEAD_LOCAL, n_shard, T, k_tile)), tile order.
+ *   out_logits  M x K_s fp32 exact W[id].h.
+ *   out_stats   M x 2 fp32: (max_j logits/T, sum_j exp(logits/T - max)).
+ * Workspace: lmhead_shard_workspace_size bytes, 256-byte aligned. Errors as
+ * for lmhead_two_stage; token_ids_shard and row_of_id are required, and an
+ * id whose row_of_id is -1 is a bad id (NaN logit, LMHEAD_ERR_DEVICE_CHECK).
+ */
+size_t lmhead_shard_workspace_size(int64_t n_shard, int d, int r, int M, int T, int k_tile);
+int lmhead_shard_two_stage(const lmhead_bf16* W_shard, const lmhead_bf16* A_shard,
+                           const lmhead_bf16* B, const lmhead_bf16* h,
+                           const int32_t* token_ids_shard, const int32_t* row_of_id,
+                           int64_t n_vocab, int64_t n_shard, int d, int r, int M, int T,
+                           int k_tile, float temperature, int32_t* out_ids, float* out_logits,
+                           float* out_stats, void* workspace, size_t workspace_bytes,
+                           lmhead_stream stream);
+
+/*
+ * The draft distribution of one shard's candidates from every shard's stats:
+ *   all_stats  G x M x 2 fp32 (the shards' out_stats, in any shard order).
+ *   logits     M x K fp32 this shard's out_logits; out_q M x K fp32 (may
+ *              alias logits): exp(logits/T - Mx) / Z with Mx the largest of
+ *              the shards' maxima and Z = sum_g sum_g exp(max_g - Mx), so that
+ *              the shards' q together are the softmax over all candidates.
+ */
+int lmhead_shard_softmax(const float* all_stats, int G, const float* logits, int M, int K,
+                         float temperature, float* out_q, lmhead_stream stream);
 
 /*
  * Test hook for the timeout path (the pages have no counterpart). Every wait

@@ -76,6 +76,26 @@ def test_global_select_long_rows(L):
         P.check_ids("global", host(ids), S, case["tok"], C, slack_pos=SL)
 
 
+@pytest.mark.parametrize("M", [1, 3])
+def test_global_select_all_scores_tied(L, M):
+    # every row of A equal: all scores tie, so the Top-C is exactly the C
+    # smallest vocabulary ids, in ascending order (rows long enough for the
+    # several-CTAs-per-row selection)
+    import torch
+    n, r, d = 12000, 16, 64
+    case = make_case(n, d, r, M, seed=15)
+    A = np.repeat(case["A"][:1], n, axis=0)
+    tok = dev_i32(case["tok"])
+    for C in (1, 777, 4096):
+        ids, sc = L.lowrank_score_topk(L.GLOBAL, dev_bf16(A), dev_bf16(case["B"]),
+                                       dev_bf16(case["h"]), tok, C, with_scores=True)
+        ids, sc = host(ids), host(sc)
+        for m in range(M):
+            assert np.array_equal(ids[m], np.arange(C)), (C, m)
+            assert np.all(sc[m] == sc[m, 0])
+    assert L.last_device_error() == 0
+
+
 def test_scores_match_oracle(L, small):
     W, A, B, h, tok = _dev(small)
     ids, sc = L.lowrank_score_topk(L.LOCAL, A, B, h, tok, 128, 4, with_scores=True)
