@@ -72,6 +72,19 @@ bool needs_score_buffer(int mode, int k_tile) {
 // vectors, no gain at one, 1.4 us slower at eight, so it is used above eight.
 // LMHEAD_OVERLAP=0 turns it off, =2 uses it at every M (measurements only).
 constexpr int kOverlapMinM = 9;
+
+// Up to this many hidden vectors the softmax runs inside the gather: the warp
+// that finishes a row's last candidate (per-row ticket, no waiting)
+// normalises the row, saving a launch. LMHEAD_FUSED_SOFTMAX_M overrides the
+// limit (0: never; measurements only).
+int fused_softmax_max_m() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("LMHEAD_FUSED_SOFTMAX_M");
+    v = e ? atoi(e) : 8;
+  }
+  return v;
+}
 int overlap_setting() {
   static int v = -1;
   if (v < 0) {
@@ -373,13 +386,17 @@ static int two_stage_impl(int mode, const lmhead_bf16* W, const lmhead_bf16* A,
   const int K = (int)candidate_count(mode, n, C_or_tile, k_tile);
   // stage 2: exact logits of the candidates (block by block as the scoring
   // kernel finishes them, when it publishes ready counters), then their
-  // softmax (one CTA per row)
-  cudaError_t e = launch_gather_logits(W, h, out_ids, n, d, M, K, out_logits, nullptr, 1.f,
-                                       nullptr, device_error_word(), s,
+  // softmax: inside the gather for a few hidden vectors (per-row tickets,
+  // zeroed by K1), else one CTA per row
+  const bool fuse = M <= fused_softmax_max_m();
+  cudaError_t e = launch_gather_logits(W, h, out_ids, n, d, M, K, out_logits,
+                                       fuse ? out_q : nullptr, 1.f / temperature,
+                                       fuse ? reinterpret_cast<int*>(ws + L.tickets) : nullptr,
+                                       device_error_word(), s,
                                        mode == LMHEAD_LOCAL ? gather_span(k_tile) : 0, ready,
                                        k_tile, (n + C_or_tile - 1) / C_or_tile);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
-  e = launch_row_softmax(out_logits, M, K, 1.f / temperature, out_q, s);
+  if (!fuse) e = launch_row_softmax(out_logits, M, K, 1.f / temperature, out_q, s);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   return LMHEAD_OK;
 }

@@ -261,17 +261,40 @@ project_u_gemv_kernel(const bf16_t* __restrict__ B, const bf16_t* __restrict__ h
 
 cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int M, bf16_t* u,
                              int* zero_ptr, int zero_ints, cudaStream_t s) {
-  cudaError_t e = cudaSuccess;
   if (M <= kGemvMaxM && d <= 8192) {
+    // templates by d (16-byte pieces per thread) and by the batch (1, 2, 4 or 8
+    // hidden vectors in registers: a one-vector call keeps its register count
+    // low, so the scoring kernel's CTAs fit beside it and start streaming A)
     const int vpt = (d + 1023) / 1024;
-    if (vpt <= 1) e = launch_kernel(false, project_u_gemv_kernel<1, 8>, dim3(r), dim3(kGemvThreads), 0, s, B, h, d, r, M, u, zero_ptr, zero_ints);
-    else if (vpt <= 2) e = launch_kernel(false, project_u_gemv_kernel<2, 8>, dim3(r), dim3(kGemvThreads), 0, s, B, h, d, r, M, u, zero_ptr, zero_ints);
-    else if (vpt <= 4) e = launch_kernel(false, project_u_gemv_kernel<4, 8>, dim3(r), dim3(kGemvThreads), 0, s, B, h, d, r, M, u, zero_ptr, zero_ints);
-    else if (M <= 4) e = launch_kernel(false, project_u_gemv_kernel<8, 4>, dim3(r), dim3(kGemvThreads), 0, s, B, h, d, r, M, u, zero_ptr, zero_ints);
-    else goto tensor_cores;
-    return e;
+    const int mm = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
+#define PG(V, MM) \
+  return launch_kernel(false, project_u_gemv_kernel<V, MM>, dim3(r), dim3(kGemvThreads), 0, s, B, h, \
+                       d, r, M, u, zero_ptr, zero_ints)
+    if (vpt <= 1) {
+      if (mm == 1) PG(1, 1);
+      if (mm == 2) PG(1, 2);
+      if (mm == 4) PG(1, 4);
+      PG(1, 8);
+    }
+    if (vpt <= 2) {
+      if (mm == 1) PG(2, 1);
+      if (mm == 2) PG(2, 2);
+      if (mm == 4) PG(2, 4);
+      PG(2, 8);
+    }
+    if (vpt <= 4) {
+      if (mm == 1) PG(4, 1);
+      if (mm == 2) PG(4, 2);
+      if (mm == 4) PG(4, 4);
+      PG(4, 8);
+    }
+    if (mm <= 4) {
+      if (mm == 1) PG(8, 1);
+      if (mm == 2) PG(8, 2);
+      PG(8, 4);
+    }
+#undef PG
   }
-tensor_cores:
   if (d <= kProjTcMaxD) {
     // d split over a cluster of KS <= 8 CTAs, slices of a multiple of 64 columns
     const int KS = min(8, (d + 511) / 512);
@@ -284,7 +307,7 @@ tensor_cores:
         !make_bf16_map(&bmap, B, (uint64_t)r, (uint64_t)d, kTcN, 64))
       return cudaErrorInvalidValue;
     static int smem_set[64] = {0};
-    e = ensure_dynamic_smem(project_u_tc_kernel, smem, smem_set);
+    cudaError_t e = ensure_dynamic_smem(project_u_tc_kernel, smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(KS, (r + kTcN - 1) / kTcN, (M + kTcHid - 1) / kTcHid);
