@@ -55,8 +55,9 @@ struct Layout {
   bool ms = false;  // global Top-C through several CTAs per row
 };
 
+// The fused scoring kernel of local mode: one or two hidden vectors take the
+// warp-per-row GEMV kernel, more the tensor cores, where each applies.
 bool use_tc(int mode, int r, int T, int k_tile, int M) {
-  // small batches take the CUDA-core GEMV kernel where it applies
   return mode == LMHEAD_LOCAL && local_topk_tc_supported(r, T, k_tile) &&
          !local_topk_gemv_supported(M, r, T, k_tile);
 }
@@ -73,15 +74,17 @@ bool needs_score_buffer(int mode, int k_tile) {
 // LMHEAD_OVERLAP=0 turns it off, =2 uses it at every M (measurements only).
 constexpr int kOverlapMinM = 9;
 
-// Up to this many hidden vectors the softmax runs inside the gather: the warp
-// that finishes a row's last candidate (per-row ticket, no waiting)
-// normalises the row, saving a launch. LMHEAD_FUSED_SOFTMAX_M overrides the
-// limit (0: never; measurements only).
+// Up to this many hidden vectors the softmax can run inside the gather: the
+// warp that finishes a row's last candidate (per-row ticket, no waiting)
+// normalises the row, saving a launch. Measured on the 128256-row head it is
+// slower (one hidden vector 25.4 -> 35.7 us, eight 47.7 -> 59.9 us: every
+// gather warp waits on its ticket's round trip and one warp normalises the
+// row), so it is off; LMHEAD_FUSED_SOFTMAX_M sets the limit (measurements).
 int fused_softmax_max_m() {
   static int v = -1;
   if (v < 0) {
     const char* e = getenv("LMHEAD_FUSED_SOFTMAX_M");
-    v = e ? atoi(e) : 8;
+    v = e ? atoi(e) : 0;
   }
   return v;
 }
@@ -220,8 +223,12 @@ int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
     if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
     return LMHEAD_OK;
   }
+  // score writeback: the GEMV kernel for one or two hidden vectors, else the
+  // tensor-core row products
   float* S = reinterpret_cast<float*>(ws + L.scores);
-  e = launch_rows_dense_tc(A, n, r, u, M, S, n, device_error_word(), s);
+  e = local_topk_gemv_supported(M, r, 256, 1) ? launch_scores_gemv(A, u, n, r, M, S, s)
+                                               : launch_rows_dense_tc(A, n, r, u, M, S, n,
+                                                                      device_error_word(), s);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   const int64_t seg = mode == LMHEAD_GLOBAL ? n : C_or_tile;
   const int k = mode == LMHEAD_GLOBAL ? C_or_tile : k_tile;

@@ -10,6 +10,7 @@
 // ticket, no waiting) computes that row's softmax and resets the ticket.
 // K6 standalone: one CTA per row, any row length.
 #include <math.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -19,6 +20,7 @@ namespace lmhead {
 namespace {
 
 constexpr int kWarpsPerCta = 8;
+constexpr int kGatherMinCtas = 6;  // CTAs per SM the register budget is sized for
 
 // Online max/sum over a row, lane-strided, then combined across the warp.
 __device__ __forceinline__ void warp_row_softmax(const float* L, float* q, int K,
@@ -75,7 +77,11 @@ __device__ __forceinline__ uint32_t candidate_of(uint32_t c, uint32_t M, uint32_
 // input), so only the W row streams through L1 per candidate. Measured on the
 // n=128256, d=4096, M=64 workload: 8 warps, 4 loads, 6 CTAs per SM (48 warps)
 // with staging is the fastest of the shapes tried (4-16 warps, 2-16 loads).
-template <int WPC, int UNR, int MINB, bool SH>
+// FUSED: the softmax-in-gather path (q, tickets) is compiled in; ROWMAP: ids
+// are mapped to W rows through row_of_id (a vocabulary shard); OVL: the
+// warps wait on the scoring kernel's ready counters. Without them (the usual
+// case) the kernel needs fewer registers.
+template <int WPC, int UNR, int MINB, bool SH, bool FUSED, bool ROWMAP, bool OVL>
 __global__ void __launch_bounds__(WPC * 32, MINB)
 gather_logits_kernel(const bf16_t* __restrict__ W, const bf16_t* __restrict__ h,
                      const int32_t* __restrict__ ids, int64_t n, int d, int M, int K,
@@ -105,11 +111,11 @@ gather_logits_kernel(const bf16_t* __restrict__ W, const bf16_t* __restrict__ h,
   }
   // ids come from the previous kernel: wait for all of it, or (ready) only
   // for the block of tiles that holds this warp's candidate
-  if (!ready) pdl_wait();
+  if (!OVL) pdl_wait();
   if (c >= MK) return;
   int m;
   const uint32_t flat = candidate_of(c, M, K, span, &m);
-  if (ready) {
+  if (OVL) {
     if (lane == 0) {
       const int b = (int)((flat - (uint32_t)m * (uint32_t)K) / (uint32_t)k_tile) / kReadyTiles;
       wait_count(ready + b, min(kReadyTiles, tiles - b * kReadyTiles) * M,
@@ -117,11 +123,13 @@ gather_logits_kernel(const bf16_t* __restrict__ W, const bf16_t* __restrict__ h,
     }
     __syncwarp();
   }
-  const int32_t id = __ldcg(ids + flat);
+  // overlapping the scoring kernel, ids may be written while this CTA runs:
+  // read them from L2; otherwise through L1, where a CTA's warps share a line
+  const int32_t id = OVL ? __ldcg(ids + flat) : __ldg(ids + flat);
   // the W row of the id: the id itself, or (a vocabulary shard) its local row
   int64_t row = id;
   bool bad = id < 0 || (int64_t)id >= n;
-  if (!bad && row_of_id) {
+  if (ROWMAP && !bad) {
     row = __ldg(row_of_id + id);
     bad = row < 0 || row >= n_rows;
   }
@@ -143,6 +151,7 @@ gather_logits_kernel(const bf16_t* __restrict__ W, const bf16_t* __restrict__ h,
     s = warp_sum(acc);
   }
   if (lane == 0) logits[flat] = s;
+  if constexpr (!FUSED) return;
   if (q == nullptr) return;
   int ticket = 0;
   if (lane == 0) {
@@ -305,7 +314,16 @@ row_softmax_reg_kernel(const float* __restrict__ L, int K, float inv_temp, float
 
 }  // namespace
 
-template <int WPC, int UNR, int MINB, bool SH>
+int overlap_ctas() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("LMHEAD_GATHER_OVL_CTAS");
+    v = e ? atoi(e) : kGatherMinCtas;
+  }
+  return v;
+}
+
+template <int WPC, int UNR, int MINB, bool SH, bool FUSED, bool ROWMAP, bool OVL>
 cudaError_t launch_gather_v(const bf16_t* W, const bf16_t* h, const int32_t* ids, int64_t n, int d,
                             int M, int K, float* logits, float* q, float inv_temp, int* tickets,
                             int* err, cudaStream_t s, int span, const int* ready, int k_tile,
@@ -315,10 +333,11 @@ cudaError_t launch_gather_v(const bf16_t* W, const bf16_t* h, const int32_t* ids
   const size_t smem = SH ? (size_t)d * 2 : 0;
   static int smem_set[64] = {0};
   if (SH) {
-    cudaError_t e = ensure_dynamic_smem(gather_logits_kernel<WPC, UNR, MINB, SH>, smem, smem_set);
+    cudaError_t e =
+        ensure_dynamic_smem(gather_logits_kernel<WPC, UNR, MINB, SH, FUSED, ROWMAP, OVL>, smem, smem_set);
     if (e != cudaSuccess) return e;
   }
-  return launch_kernel(true, gather_logits_kernel<WPC, UNR, MINB, SH>, dim3(grid),
+  return launch_kernel(true, gather_logits_kernel<WPC, UNR, MINB, SH, FUSED, ROWMAP, OVL>, dim3(grid),
                        dim3(WPC * 32), smem, s, W, h, ids, n, d, M, K, span, logits, q,
                        inv_temp, tickets, err, ready, k_tile, (int)tiles, row_of_id, n_rows);
 }
@@ -329,9 +348,24 @@ cudaError_t launch_gather_logits(const bf16_t* W, const bf16_t* h, const int32_t
                                  const int* ready, int k_tile, int64_t tiles,
                                  const int32_t* row_of_id, int64_t n_rows) {
   if (ready && (k_tile < 1 || tiles < 1)) return cudaErrorInvalidValue;
-  return launch_gather_v<kWarpsPerCta, 4, 6, true>(W, h, ids, n, d, M, K, logits, q, inv_temp,
-                                                     tickets, err, s, span, ready, k_tile, tiles,
-                                                     row_of_id, n_rows);
+#define GATHER(MINB, FUSED, ROWMAP, OVL)                                                  \
+  return launch_gather_v<kWarpsPerCta, 4, MINB, true, FUSED, ROWMAP, OVL>(                 \
+      W, h, ids, n, d, M, K, logits, q, inv_temp, tickets, err, s, span, ready, k_tile, tiles, \
+      row_of_id, n_rows)
+  if (q) GATHER(6, true, false, false);  // softmax fused (the no-allocation entry point)
+  if (row_of_id) {                       // a vocabulary shard
+    if (ready) GATHER(6, false, true, true);
+    GATHER(6, false, true, false);
+  }
+  if (ready) {
+    // overlapping the scoring kernel, the gather's CTAs share SMs with it and
+    // registers bound how many fit; LMHEAD_GATHER_OVL_CTAS=8 compiles the
+    // kernel for eight CTAs per SM (32 registers, some spilled; measurements)
+    if (overlap_ctas() == 8) GATHER(8, false, false, true);
+    GATHER(kGatherMinCtas, false, false, true);
+  }
+  GATHER(6, false, false, false);
+#undef GATHER
 }
 
 cudaError_t launch_row_softmax(const float* L, int M, int64_t K, float inv_temp, float* q,

@@ -27,6 +27,11 @@ cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int
 // r = 256) it runs the warp-per-row GEMV kernel.
 constexpr int kLocalGemvMaxM = 2;
 bool local_topk_gemv_supported(int M, int r, int T, int k_tile);
+// The same GEMV kernel writing every score to S (M x n fp32 by position)
+// instead of selecting: the global path's writeback for one or two hidden
+// vectors at r = 256.
+cudaError_t launch_scores_gemv(const bf16_t* A, const bf16_t* u, int64_t n, int r, int M, float* S,
+                               cudaStream_t s);
 // ready: the gather's ready counters (GEMV kernel only; may be nullptr).
 cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
                                   int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,

@@ -177,12 +177,15 @@ __device__ __forceinline__ bool gemv_beats(float sa, int32_t ia, float sb, int32
 
 // DB: the next batch of rows is requested before the current one is used
 // (more registers, so fewer CTAs per SM).
-template <int MB, int KT, bool DB>
+// WB: write the scores to S (M x n by position: the global path's score
+// writeback) instead of selecting.
+template <int MB, int KT, bool DB, bool WB = false>
 __global__ void __launch_bounds__(kGemvThreads, DB ? (MB == 1 ? 3 : 2) : (MB == 1 ? 4 : 3))
 local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u,
                        const int32_t* __restrict__ token_ids, int64_t n, int r, int M, int T,
                        int k_tile, int K, int32_t* __restrict__ out_ids,
-                       float* __restrict__ out_scores, int* __restrict__ ready) {
+                       float* __restrict__ out_scores, int* __restrict__ ready,
+                       float* __restrict__ S = nullptr) {
   __shared__ float sc[MB][kGemvThreads];
   __shared__ int32_t svid[kGemvThreads];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -246,6 +249,13 @@ local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ 
     }
   }
   cta_sync();
+  if constexpr (WB) {  // the global path: every score to HBM, rows in position order
+    for (int i = tid; i < mb * kGemvThreads; i += kGemvThreads) {
+      const int mm = i / kGemvThreads, rl = i - mm * kGemvThreads;
+      if (row0 + rl < n) S[(size_t)(m0 + mm) * n + row0 + rl] = sc[mm][rl];
+    }
+    return;
+  }
   // one warp per (tile, hidden vector)
   const int tpc = kGemvThreads / T;
   const int jobs = tpc * mb;
@@ -316,7 +326,8 @@ cudaError_t launch_gemv_mb(const bf16_t* A, const bf16_t* u, const int32_t* toke
   dim3 grid((unsigned)((n + kGemvThreads - 1) / kGemvThreads), (unsigned)((M + MB - 1) / MB));
 #define GV(KT)                                                                                \
   return launch_kernel(true, local_topk_gemv_kernel<MB, KT, DB>, grid, dim3(kGemvThreads), 0, s, \
-                       A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, ready);
+                       A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, ready,  \
+                       (float*)nullptr);
   if (k_tile <= 1) GV(1);
   if (k_tile <= 2) GV(2);
   if (k_tile <= 4) GV(4);
@@ -335,6 +346,19 @@ bool gemv_enabled() {
 }
 
 }  // namespace
+
+cudaError_t launch_scores_gemv(const bf16_t* A, const bf16_t* u, int64_t n, int r, int M, float* S,
+                               cudaStream_t s) {
+  if (!local_topk_gemv_supported(M, r, kGemvThreads, 1)) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)((n + kGemvThreads - 1) / kGemvThreads), 1);
+  if (M <= 1)
+    return launch_kernel(true, local_topk_gemv_kernel<1, 1, false, true>, grid, dim3(kGemvThreads),
+                         0, s, A, u, (const int32_t*)nullptr, n, r, M, kGemvThreads, 1, 0,
+                         (int32_t*)nullptr, (float*)nullptr, (int*)nullptr, S);
+  return launch_kernel(true, local_topk_gemv_kernel<2, 1, true, true>, grid, dim3(kGemvThreads), 0,
+                       s, A, u, (const int32_t*)nullptr, n, r, M, kGemvThreads, 1, 0,
+                       (int32_t*)nullptr, (float*)nullptr, (int*)nullptr, S);
+}
 
 bool local_topk_gemv_supported(int M, int r, int T, int k_tile) {
   return gemv_enabled() && M <= kLocalGemvMaxM && r == 256 && T >= 32 &&

@@ -46,6 +46,7 @@ constexpr int kKBlock = 64;                 // bf16 per 128-byte swizzled row
 constexpr int kStageBytes = kChunk * 128;   // one 128-row x 64-element box
 constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kMaxStages = 12;
+constexpr int kOverlapStages = 3;           // ring depth when the gather overlaps
 constexpr int kAcc = 4;                     // TMEM accumulators (the MMA runs ahead)
 constexpr int kTmemCols = kAcc * 128;       // 128 fp32 columns each
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kHid, kChunk);
@@ -875,6 +876,17 @@ local_topk_tc_dyn_kernel(const __grid_constant__ CUtensorMap amap,
 }
 
 // ---------------------------------------------------------------- host side
+// LMHEAD_K4_STAGES = s caps the ring at s stages (measurements only: a
+// smaller ring leaves shared memory for more gather CTAs beside each CTA).
+int stage_cap() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("LMHEAD_K4_STAGES");
+    v = e ? atoi(e) : 0;
+  }
+  return v;
+}
+
 // LMHEAD_K4_CHUNK = 128 keeps 128-row MMAs for every tile (measurements only).
 bool chunk256_enabled() {
   static int v = -1;
@@ -957,6 +969,12 @@ cudaError_t launch_local_topk_tc(const bf16_t* A, const bf16_t* u, const int32_t
   const size_t st_bytes = (size_t)ch * 128;
   int stages = (int)((budget - 1024 - u_bytes - xchg_bytes) / st_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
+  // With the gather overlapping this kernel, three stages: the 32 KB given
+  // up lets a gather CTA more sit beside each of these CTAs (four instead of
+  // two, then bound by registers), worth more than the fourth stage (the
+  // 128256-row head at 64 hidden vectors: 109.2 -> 98.5 us per call).
+  const int cap = stage_cap() >= 2 ? stage_cap() : (ready && T % kChunk == 0 ? kOverlapStages : 0);
+  if (cap >= 2 && stages > cap) stages = cap;
   if (stages < 2) return cudaErrorInvalidValue;
   p.stages = stages;
   p.R = (T % kChunk == 0) ? (M <= 32 ? 4 : (M <= 64 ? 2 : 1)) : 1;

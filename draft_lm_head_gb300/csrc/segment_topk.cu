@@ -168,18 +168,22 @@ segment_topk_kernel(const float* __restrict__ S, const int32_t* __restrict__ tok
 // ---------------------------------------------------------------- long rows, few rows
 // Global Top-k of rows too long for one CTA to sweep quickly (one CTA per row
 // does every radix pass over the whole row: ~100 us at n = 128256). Here G
-// CTAs share a row. Pass kernels (up to six launches, 12-bit digits from the
+// CTAs share a row. Pass kernels (kMsPasses launches, 12-bit digits from the
 // top of the key): each CTA histograms the keys of its segment that lie in
 // the row's current range [lo, hi] and adds the histogram into the row's
 // global one; the last CTA of the row to finish (atomic ticket, no waiting)
 // finds the boundary digit, narrows [lo, hi], counts the keys above it and
-// marks the row done once the range holds at most kCap keys. Later passes of
-// a done row return at once. Collection kernel: every CTA appends its keys
-// above the range and inside it to two per-row lists; the last CTA sorts the
+// marks the row done once the range holds at most kCap keys (fp32 scores
+// need one pass in practice: a 12-bit digit is a sign, the exponent and
+// three mantissa bits). Collection kernel: every CTA appends its keys above
+// the range and inside it to two per-row lists; the last CTA sorts the
 // survivors (at most k + kCap keys) and writes the row's Top-k, score
-// descending, ties by the smaller vocabulary id (the keys are unique).
+// descending, ties by the smaller vocabulary id (the keys are unique). A row
+// the passes left unfinished (more than kCap keys sharing 24 key bits) is
+// finished by the collection kernel's last CTA alone, with the remaining
+// passes over the whole row.
 constexpr int kMsThreads = 1024;
-constexpr int kMsPasses = 6;      // 64-bit keys, 12-bit digits (the last ones overlap)
+constexpr int kMsPasses = 2;      // launched passes; later digits in the fallback
 constexpr int kMsStateInts = 16;  // per-row state, then the row's kBins histogram
 
 struct MsState {
@@ -192,7 +196,48 @@ struct MsState {
 };
 static_assert(sizeof(MsState) <= kMsStateInts * sizeof(int), "state slot");
 
+struct MsBoundary {
+  unsigned long long lo, hi;
+  int above, count;
+};
+
 __device__ __forceinline__ int64_t ms_seg(int64_t n, int G) { return (n + G - 1) / G; }
+__device__ __forceinline__ int ms_shift(int pass) { return max(0, 64 - kDigit * (pass + 1)); }
+
+// Every thread of the CTA (kMsThreads): with hist[] the kBins counts of the
+// keys in [lo, hi] by the digit at `shift`, find the bin holding the need-th
+// largest such key; thread that finds it writes *out (the narrowed range, the
+// keys above the bin, the bin's count).
+__device__ void ms_boundary(const uint32_t* hist, uint32_t* part, uint32_t need, int shift,
+                            uint64_t lo, MsBoundary* out) {
+  const int tid = threadIdx.x;
+  const int g = kMsThreads - 1 - tid;  // thread tid owns bins [4g, 4g+4), descending order
+  const uint32_t local = hist[4 * g] + hist[4 * g + 1] + hist[4 * g + 2] + hist[4 * g + 3];
+  part[tid] = local;
+  cta_sync();
+  for (int off = 1; off < kMsThreads; off <<= 1) {
+    const uint32_t v = tid >= off ? part[tid - off] : 0u;
+    cta_sync();
+    part[tid] += v;
+    cta_sync();
+  }
+  uint32_t above = part[tid] - local;
+  if (above < need && above + local >= need) {
+    for (int b = 4 * g + 3; b >= 4 * g; --b) {
+      if (above + hist[b] >= need) {
+        const uint64_t prefix = lo & ~((((uint64_t)kBins - 1) << shift) | ((1ull << shift) - 1ull));
+        const uint64_t nlo = prefix | ((uint64_t)b << shift);
+        out->lo = nlo;
+        out->hi = nlo | ((1ull << shift) - 1ull);
+        out->above = (int)above;
+        out->count = (int)hist[b];
+        break;
+      }
+      above += hist[b];
+    }
+  }
+  cta_sync();
+}
 
 // grid (G, M). `zero`: M x (kMsStateInts + kBins) ints, zero before the
 // first pass of a call.
@@ -201,6 +246,7 @@ ms_pass_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_id
                int k, int* __restrict__ zero) {
   __shared__ uint32_t hist[kBins];
   __shared__ uint32_t part[kMsThreads];
+  __shared__ MsBoundary bnd;
   __shared__ int s_last;
   const int tid = threadIdx.x, G = gridDim.x, m = blockIdx.y;
   int* zr = zero + (size_t)m * (kMsStateInts + kBins);
@@ -212,7 +258,7 @@ ms_pass_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_id
   const int pass = st->pass;
   const uint64_t lo = pass ? st->lo : 0ull, hi = pass ? st->hi : ~0ull;
   const int gt = st->gt;
-  const int shift = max(0, 64 - kDigit * (pass + 1));
+  const int shift = ms_shift(pass);
   const int64_t per = ms_seg(n, G);
   const int64_t p0 = (int64_t)blockIdx.x * per, p1 = min(n, p0 + per);
   const float* row = S + (size_t)m * n;
@@ -237,79 +283,119 @@ ms_pass_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_id
     ghist[i] = 0;  // ready for the next pass
   }
   cta_sync();
-  const int g = kMsThreads - 1 - tid;  // thread tid owns bins [4g, 4g+4), descending order
-  const uint32_t local = hist[4 * g] + hist[4 * g + 1] + hist[4 * g + 2] + hist[4 * g + 3];
-  part[tid] = local;
-  cta_sync();
-  for (int off = 1; off < kMsThreads; off <<= 1) {
-    const uint32_t v = tid >= off ? part[tid - off] : 0u;
-    cta_sync();
-    part[tid] += v;
-    cta_sync();
-  }
-  uint32_t above = part[tid] - local;
-  const uint32_t need = (uint32_t)(min((int64_t)k, n) - gt);
-  if (above < need && above + local >= need) {
-    for (int b = 4 * g + 3; b >= 4 * g; --b) {
-      if (above + hist[b] >= need) {
-        const uint64_t prefix =
-            lo & ~((((uint64_t)kBins - 1) << shift) | ((1ull << shift) - 1ull));
-        const uint64_t nlo = prefix | ((uint64_t)b << shift);
-        st->lo = nlo;
-        st->hi = nlo | ((1ull << shift) - 1ull);
-        st->gt = gt + (int)above;
-        st->done = (hist[b] <= (uint32_t)kCap || shift == 0) ? 1 : 0;
-        break;
-      }
-      above += hist[b];
-    }
-  }
+  ms_boundary(hist, part, (uint32_t)(min((int64_t)k, n) - gt), shift, lo, &bnd);
   if (tid == 0) {
+    st->lo = bnd.lo;
+    st->hi = bnd.hi;
+    st->gt = gt + bnd.above;
+    st->done = (bnd.count <= kCap || shift == 0) ? 1 : 0;
     st->pass = pass + 1;
     st->ticket = 0;
   }
 }
 
-// grid (G, M); dynamic shared memory: the last CTA's sort buffer.
+// grid (G, M); dynamic shared memory: the last CTA's sort buffer (2 kCap
+// keys), then a histogram and scan space for the fallback passes.
 __global__ void __launch_bounds__(kMsThreads)
 ms_collect_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_ids, int64_t n,
                   int k, int* __restrict__ zero, uint64_t* __restrict__ sel,
                   uint64_t* __restrict__ cand, int32_t* __restrict__ out_ids,
                   float* __restrict__ out_scores) {
   extern __shared__ uint64_t keys[];
-  __shared__ int s_last;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(keys + 2 * kCap);
+  uint32_t* part = hist + kBins;
+  __shared__ MsBoundary bnd;
+  __shared__ int s_last, s_sel, s_cand;
   const int tid = threadIdx.x, G = gridDim.x, m = blockIdx.y;
   MsState* st = reinterpret_cast<MsState*>(zero + (size_t)m * (kMsStateInts + kBins));
   pdl_wait();
   pdl_trigger();
-  const uint64_t lo = st->lo, hi = st->hi;
+  const bool done = st->done != 0;
+  uint64_t lo = st->lo, hi = st->hi;
   const int kk = (int)min((int64_t)k, n);
   uint64_t* rsel = sel + (size_t)m * k;
   uint64_t* rcand = cand + (size_t)m * kCap;
-  const int64_t per = ms_seg(n, G);
-  const int64_t p0 = (int64_t)blockIdx.x * per, p1 = min(n, p0 + per);
   const float* row = S + (size_t)m * n;
-  for (int64_t p = p0 + tid; p < p1; p += kMsThreads) {
-    const uint64_t key = key_at(row, token_ids, p);
-    if (key > hi) {
-      const int i = atomicAdd(&st->n_sel, 1);
-      if (i < kk) rsel[i] = key;
-    } else if (key >= lo) {
-      const int i = atomicAdd(&st->n_cand, 1);
-      if (i < kCap) rcand[i] = key;
+  if (done) {
+    const int64_t per = ms_seg(n, G);
+    const int64_t p0 = (int64_t)blockIdx.x * per, p1 = min(n, p0 + per);
+    for (int64_t p = p0 + tid; p < p1; p += kMsThreads) {
+      const uint64_t key = key_at(row, token_ids, p);
+      if (key > hi) {
+        const int i = atomicAdd(&st->n_sel, 1);
+        if (i < kk) rsel[i] = key;
+      } else if (key >= lo) {
+        const int i = atomicAdd(&st->n_cand, 1);
+        if (i < kCap) rcand[i] = key;
+      }
     }
+    __threadfence();
   }
-  __threadfence();
   cta_sync();
   if (tid == 0) s_last = atomicAdd(&st->ticket, 1) == G - 1;
   cta_sync();
   if (!s_last) return;
   __threadfence();
-  const int ns = min(__ldcg(&st->n_sel), kk), nc = min(__ldcg(&st->n_cand), kCap);
-  const int P = pow2_at_least(ns + nc);
-  for (int i = tid; i < P; i += kMsThreads)
-    keys[i] = i < ns ? __ldcg(rsel + i) : (i < ns + nc ? __ldcg(rcand + i - ns) : 0ull);
+  int ns, nc;
+  if (done) {
+    ns = min(__ldcg(&st->n_sel), kk);
+    nc = min(__ldcg(&st->n_cand), kCap);
+    const int P = pow2_at_least(ns + nc);
+    for (int i = tid; i < P; i += kMsThreads)
+      keys[i] = i < ns ? __ldcg(rsel + i) : (i < ns + nc ? __ldcg(rcand + i - ns) : 0ull);
+  } else {
+    // fallback: the remaining passes over the whole row by this CTA alone
+    int gt = st->gt;
+    for (int pass = st->pass;; ++pass) {
+      const int shift = ms_shift(pass);
+      for (int i = tid; i < kBins; i += kMsThreads) hist[i] = 0;
+      cta_sync();
+      for (int64_t p = tid; p < n; p += kMsThreads) {
+        const uint64_t key = key_at(row, token_ids, p);
+        if (key >= lo && key <= hi) atomicAdd(&hist[(key >> shift) & (kBins - 1)], 1u);
+      }
+      cta_sync();
+      ms_boundary(hist, part, (uint32_t)(kk - gt), shift, lo, &bnd);
+      lo = bnd.lo;
+      hi = bnd.hi;
+      gt += bnd.above;
+      const int count = bnd.count;
+      cta_sync();
+      if (count <= kCap || shift == 0) break;
+    }
+    if (tid == 0) { s_sel = 0; s_cand = 0; }
+    cta_sync();
+    for (int64_t p = tid; p < n; p += kMsThreads) {
+      const uint64_t key = key_at(row, token_ids, p);
+      if (key > hi) {
+        const int i = atomicAdd(&s_sel, 1);
+        if (i < kk) keys[i] = key;
+      } else if (key >= lo) {
+        const int i = atomicAdd(&s_cand, 1);
+        if (i < kCap) keys[kCap + i] = key;
+      }
+    }
+    cta_sync();
+    ns = min(s_sel, kk);
+    nc = min(s_cand, kCap);
+    // move the candidates next to the selected keys (read all, then write)
+    uint64_t mv[kCap / kMsThreads];
+#pragma unroll
+    for (int r = 0; r < kCap / kMsThreads; ++r) {
+      const int i = tid + r * kMsThreads;
+      mv[r] = i < nc ? keys[kCap + i] : 0ull;
+    }
+    cta_sync();
+#pragma unroll
+    for (int r = 0; r < kCap / kMsThreads; ++r) {
+      const int i = tid + r * kMsThreads;
+      if (i < nc) keys[ns + i] = mv[r];
+    }
+    const int P = pow2_at_least(ns + nc);
+    for (int i = ns + nc + tid; i < P; i += kMsThreads) keys[i] = 0ull;
+  }
   cta_sync();
+  const int P = pow2_at_least(ns + nc);
   bitonic_desc(keys, P);
   const int take = min(kk, ns + nc);
   for (int j = tid; j < take; j += kMsThreads) {
@@ -349,7 +435,8 @@ cudaError_t launch_row_select_multi(const float* S, const int32_t* token_ids, in
   }
   uint64_t* sel = static_cast<uint64_t*>(scratch);
   uint64_t* cand = sel + (size_t)M * k;
-  const size_t smem = (size_t)2 * kCap * sizeof(uint64_t);  // k + kCap <= 2 kCap keys
+  // k + kCap <= 2 kCap keys, then the fallback's histogram and scan space
+  const size_t smem = (size_t)2 * kCap * sizeof(uint64_t) + (kBins + kMsThreads) * sizeof(uint32_t);
   static int smem_set[64] = {0};
   cudaError_t e = ensure_dynamic_smem(ms_collect_kernel, smem, smem_set);
   if (e != cudaSuccess) return e;
