@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kWarpsPerCta = 8;
 constexpr int kGatherMinCtas = 6;  // CTAs per SM the register budget is sized for
+constexpr int kSmallGatherPerSm = 2 * kWarpsPerCta;  // candidates per SM of a "small" gather
 
 // Online max/sum over a row, lane-strided, then combined across the warp.
 __device__ __forceinline__ void warp_row_softmax(const float* L, float* q, int K,
@@ -348,14 +349,23 @@ cudaError_t launch_gather_logits(const bf16_t* W, const bf16_t* h, const int32_t
                                  const int* ready, int k_tile, int64_t tiles,
                                  const int32_t* row_of_id, int64_t n_rows) {
   if (ready && (k_tile < 1 || tiles < 1)) return cudaErrorInvalidValue;
-#define GATHER(MINB, FUSED, ROWMAP, OVL)                                                  \
-  return launch_gather_v<kWarpsPerCta, 4, MINB, true, FUSED, ROWMAP, OVL>(                 \
+#define GATHER_U(UNR, MINB, FUSED, ROWMAP, OVL)                                           \
+  return launch_gather_v<kWarpsPerCta, UNR, MINB, true, FUSED, ROWMAP, OVL>(               \
       W, h, ids, n, d, M, K, logits, q, inv_temp, tickets, err, s, span, ready, k_tile, tiles, \
       row_of_id, n_rows)
+#define GATHER(MINB, FUSED, ROWMAP, OVL) GATHER_U(4, MINB, FUSED, ROWMAP, OVL)
   if (q) GATHER(6, true, false, false);  // softmax fused (the no-allocation entry point)
   if (row_of_id) {                       // a vocabulary shard
     if (ready) GATHER(6, false, true, true);
     GATHER(6, false, true, false);
+  }
+  if (!ready && (int64_t)M * K <= (int64_t)kSmallGatherPerSm * sm_count()) {
+    // a thousand or two candidates (one or two hidden vectors): the warps are
+    // too few to hide DRAM latency, so each lane keeps 16 loads in flight (a
+    // whole 8 KB row per warp request round) instead of 4; at 122 registers
+    // two CTAs fit per SM, so only gathers that fit one such wave take it
+    // (measured: one hidden vector 25.4 -> 23.1 us a call, eight 47.2 -> 49.8)
+    GATHER_U(16, 2, false, false, false);
   }
   if (ready) {
     // overlapping the scoring kernel, the gather's CTAs share SMs with it and
@@ -366,6 +376,7 @@ cudaError_t launch_gather_logits(const bf16_t* W, const bf16_t* h, const int32_t
   }
   GATHER(6, false, false, false);
 #undef GATHER
+#undef GATHER_U
 }
 
 cudaError_t launch_row_softmax(const float* L, int M, int64_t K, float inv_temp, float* q,

@@ -31,7 +31,12 @@ __device__ __forceinline__ uint64_t key_at(const float* __restrict__ row,
   return select_key(__ldcg(row + p), id);
 }
 
-// Sort keys[0..P) descending, P a power of two, all threads participate.
+// Sort keys[0..P) descending, P a power of two, all threads participate
+// (blockDim.x a multiple of 32). Pair i of a stage touches elements of the
+// 64-element chunk i / 32 when the stride is at most 32, and warp w handles
+// pairs w*32 + 32*blockDim.x/32*k + lane, i.e. only its own chunks: such
+// stages need only a warp barrier after them unless the next stage reaches
+// across chunks (stride 64 and up), which needs the CTA barrier.
 __device__ void bitonic_desc(uint64_t* keys, int P) {
   for (int size = 2; size <= P; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -45,9 +50,15 @@ __device__ void bitonic_desc(uint64_t* keys, int P) {
           keys[par] = a;
         }
       }
-      cta_sync();
+      const int next = stride > 1 ? stride >> 1 : size;  // the next stage's stride
+      if (stride >= 64 || next >= 64) {
+        cta_sync();
+      } else {
+        __syncwarp();
+      }
     }
   }
+  cta_sync();
 }
 
 __device__ __forceinline__ int pow2_at_least(int x) {
@@ -173,9 +184,9 @@ segment_topk_kernel(const float* __restrict__ S, const int32_t* __restrict__ tok
 // the row's current range [lo, hi] and adds the histogram into the row's
 // global one; the last CTA of the row to finish (atomic ticket, no waiting)
 // finds the boundary digit, narrows [lo, hi], counts the keys above it and
-// marks the row done once the range holds at most kCap keys (fp32 scores
-// need one pass in practice: a 12-bit digit is a sign, the exponent and
-// three mantissa bits). Collection kernel: every CTA appends its keys above
+// marks the row done once the range holds at most kMsDone keys (fp32 scores
+// need two passes in practice: the first 12-bit digit is a sign, the
+// exponent and three mantissa bits). Collection kernel: every CTA appends its keys above
 // the range and inside it to two per-row lists; the last CTA sorts the
 // survivors (at most k + kCap keys) and writes the row's Top-k, score
 // descending, ties by the smaller vocabulary id (the keys are unique). A row
@@ -185,6 +196,10 @@ segment_topk_kernel(const float* __restrict__ S, const int32_t* __restrict__ tok
 constexpr int kMsThreads = 1024;
 constexpr int kMsPasses = 2;      // launched passes; later digits in the fallback
 constexpr int kMsStateInts = 16;  // per-row state, then the row's kBins histogram
+// A row is done once its boundary range holds at most this many keys: the
+// collection's last CTA then sorts about C + kMsDone keys, not C + kCap (the
+// first digit of fp32 scores often leaves a few thousand keys in range).
+constexpr int kMsDone = 512;
 
 struct MsState {
   unsigned long long lo, hi;  // current key range (meaningful once pass > 0)
@@ -210,18 +225,31 @@ __device__ __forceinline__ int ms_shift(int pass) { return max(0, 64 - kDigit * 
 // keys above the bin, the bin's count).
 __device__ void ms_boundary(const uint32_t* hist, uint32_t* part, uint32_t need, int shift,
                             uint64_t lo, MsBoundary* out) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = kMsThreads - 1 - tid;  // thread tid owns bins [4g, 4g+4), descending order
   const uint32_t local = hist[4 * g] + hist[4 * g + 1] + hist[4 * g + 2] + hist[4 * g + 3];
-  part[tid] = local;
-  cta_sync();
-  for (int off = 1; off < kMsThreads; off <<= 1) {
-    const uint32_t v = tid >= off ? part[tid - off] : 0u;
-    cta_sync();
-    part[tid] += v;
-    cta_sync();
+  // inclusive prefix over threads (thread 0 holds the top bins): a warp scan,
+  // then a scan of the 32 warp totals by warp 0 (part[] holds them)
+  uint32_t v = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += t;
   }
-  uint32_t above = part[tid] - local;
+  if (lane == 31) part[warp] = v;
+  cta_sync();
+  if (warp == 0) {
+    const uint32_t tot = part[lane];
+    uint32_t w = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += t;
+    }
+    part[lane] = w - tot;  // keys in the bins of the warps before
+  }
+  cta_sync();
+  uint32_t above = v + part[warp] - local;  // keys in bins above this thread's
   if (above < need && above + local >= need) {
     for (int b = 4 * g + 3; b >= 4 * g; --b) {
       if (above + hist[b] >= need) {
@@ -288,7 +316,7 @@ ms_pass_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_id
     st->lo = bnd.lo;
     st->hi = bnd.hi;
     st->gt = gt + bnd.above;
-    st->done = (bnd.count <= kCap || shift == 0) ? 1 : 0;
+    st->done = (bnd.count <= kMsDone || shift == 0) ? 1 : 0;
     st->pass = pass + 1;
     st->ticket = 0;
   }
@@ -305,7 +333,7 @@ ms_collect_kernel(const float* __restrict__ S, const int32_t* __restrict__ token
   uint32_t* hist = reinterpret_cast<uint32_t*>(keys + 2 * kCap);
   uint32_t* part = hist + kBins;
   __shared__ MsBoundary bnd;
-  __shared__ int s_last, s_sel, s_cand;
+  __shared__ int s_last, s_sel, s_cand, s_base_sel, s_base_cand;
   const int tid = threadIdx.x, G = gridDim.x, m = blockIdx.y;
   MsState* st = reinterpret_cast<MsState*>(zero + (size_t)m * (kMsStateInts + kBins));
   pdl_wait();
@@ -317,18 +345,34 @@ ms_collect_kernel(const float* __restrict__ S, const int32_t* __restrict__ token
   uint64_t* rcand = cand + (size_t)m * kCap;
   const float* row = S + (size_t)m * n;
   if (done) {
+    // this CTA's keys above the range and inside it go to shared memory first
+    // (at most kk and kCap: the row's lists are no longer), then to the row's
+    // lists through one global reservation per list
+    if (tid == 0) { s_sel = 0; s_cand = 0; }
+    cta_sync();
     const int64_t per = ms_seg(n, G);
     const int64_t p0 = (int64_t)blockIdx.x * per, p1 = min(n, p0 + per);
     for (int64_t p = p0 + tid; p < p1; p += kMsThreads) {
       const uint64_t key = key_at(row, token_ids, p);
       if (key > hi) {
-        const int i = atomicAdd(&st->n_sel, 1);
-        if (i < kk) rsel[i] = key;
+        const int i = atomicAdd(&s_sel, 1);
+        if (i < kCap) keys[i] = key;
       } else if (key >= lo) {
-        const int i = atomicAdd(&st->n_cand, 1);
-        if (i < kCap) rcand[i] = key;
+        const int i = atomicAdd(&s_cand, 1);
+        if (i < kCap) keys[kCap + i] = key;
       }
     }
+    cta_sync();
+    const int ls = min(s_sel, kCap), lc = min(s_cand, kCap);
+    if (tid == 0) {
+      s_base_sel = ls ? atomicAdd(&st->n_sel, ls) : 0;
+      s_base_cand = lc ? atomicAdd(&st->n_cand, lc) : 0;
+    }
+    cta_sync();
+    for (int i = tid; i < ls; i += kMsThreads)
+      if (s_base_sel + i < kk) rsel[s_base_sel + i] = keys[i];
+    for (int i = tid; i < lc; i += kMsThreads)
+      if (s_base_cand + i < kCap) rcand[s_base_cand + i] = keys[kCap + i];
     __threadfence();
   }
   cta_sync();
