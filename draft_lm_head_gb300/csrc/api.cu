@@ -225,16 +225,20 @@ int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
   }
   // score writeback: the GEMV kernel for one or two hidden vectors, else the
   // tensor-core row products
+  // (the GEMV form also counts the multi-CTA selection's first histogram)
   float* S = reinterpret_cast<float*>(ws + L.scores);
-  e = local_topk_gemv_supported(M, r, 256, 1) ? launch_scores_gemv(A, u, n, r, M, S, s)
-                                               : launch_rows_dense_tc(A, n, r, u, M, S, n,
-                                                                      device_error_word(), s);
+  const bool gemv = local_topk_gemv_supported(M, r, 256, 1);
+  int* ms_zero = L.ms ? tickets + L.ms_at : nullptr;
+  e = gemv ? launch_scores_gemv(A, u, n, r, M, S, s,
+                                ms_zero ? ms_zero + row_select_multi_hist0(0) : nullptr,
+                                row_select_multi_hist0(1) - row_select_multi_hist0(0))
+           : launch_rows_dense_tc(A, n, r, u, M, S, n, device_error_word(), s);
   if (e != cudaSuccess || mk.mark(s) != cudaSuccess) return LMHEAD_ERR_CUDA;
   const int64_t seg = mode == LMHEAD_GLOBAL ? n : C_or_tile;
   const int k = mode == LMHEAD_GLOBAL ? C_or_tile : k_tile;
   if (L.ms)
-    e = launch_row_select_multi(S, token_ids, n, M, k, out_ids, out_scores, tickets + L.ms_at,
-                                ws + L.select, s);
+    e = launch_row_select_multi(S, token_ids, n, M, k, out_ids, out_scores, ms_zero,
+                                ws + L.select, gemv, s);
   else
     e = launch_segment_topk(S, token_ids, n, M, seg, k, out_ids, out_scores, device_error_word(),
                             s);

@@ -29,9 +29,12 @@ constexpr int kLocalGemvMaxM = 2;
 bool local_topk_gemv_supported(int M, int r, int T, int k_tile);
 // The same GEMV kernel writing every score to S (M x n fp32 by position)
 // instead of selecting: the global path's writeback for one or two hidden
-// vectors at r = 256.
+// vectors at r = 256. hist0 != nullptr: it also adds the counts of the
+// scores' top kSelectHistBits order bits of hidden vector m into
+// hist0 + m * hist0_stride (kSelectHistBins ints; the multi-CTA selection's
+// first histogram).
 cudaError_t launch_scores_gemv(const bf16_t* A, const bf16_t* u, int64_t n, int r, int M, float* S,
-                               cudaStream_t s);
+                               cudaStream_t s, int* hist0 = nullptr, int hist0_stride = 0);
 // ready: the gather's ready counters (GEMV kernel only; may be nullptr).
 cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_t* token_ids,
                                   int64_t n, int r, int M, int T, int k_tile, int32_t* out_ids,
@@ -74,13 +77,19 @@ inline int ready_words(int64_t tiles) { return ready_blocks(tiles) + 1; }  // co
 // `zero` holds row_select_multi_ints(M) ints that are zero on entry (the
 // projection kernel zeroes them), `scratch` row_select_multi_bytes(M, k)
 // bytes (no initial value). Same result and order as launch_segment_topk with
-// one segment per row.
+// one segment per row. The first histogram of row m (kSelectHistBins counts of
+// the scores' top kSelectHistBits order bits, float_key(score) >> 20) is at
+// zero + row_select_multi_hist0(m); hist0_filled: the score writeback has
+// counted it already.
+constexpr int kSelectHistBits = 12;
+constexpr int kSelectHistBins = 1 << kSelectHistBits;
 bool row_select_multi(int64_t n, int M, int k);
 int row_select_multi_ints(int M);
+int row_select_multi_hist0(int m);
 size_t row_select_multi_bytes(int M, int k);
 cudaError_t launch_row_select_multi(const float* S, const int32_t* token_ids, int64_t n, int M,
                                     int k, int32_t* out_ids, float* out_scores, int* zero,
-                                    void* scratch, cudaStream_t s);
+                                    void* scratch, bool hist0_filled, cudaStream_t s);
 
 // K5 (+K6 fused when q != nullptr): L[m,j] = W[ids[m,j]] . h[m]; q = softmax.
 // `tickets` (M ints, zero on entry, left zero on exit) enable the fusion.

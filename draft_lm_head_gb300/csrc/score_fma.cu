@@ -185,13 +185,18 @@ local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ 
                        const int32_t* __restrict__ token_ids, int64_t n, int r, int M, int T,
                        int k_tile, int K, int32_t* __restrict__ out_ids,
                        float* __restrict__ out_scores, int* __restrict__ ready,
-                       float* __restrict__ S = nullptr) {
+                       float* __restrict__ S, int* __restrict__ hist0, int hist0_stride) {
   __shared__ float sc[MB][kGemvThreads];
   __shared__ int32_t svid[kGemvThreads];
+  __shared__ uint32_t hh[WB ? MB * kSelectHistBins : 1];  // writeback: score-digit counts
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row0 = (int64_t)blockIdx.x * kGemvThreads;
   const int m0 = blockIdx.y * MB;
   const int mb = min(MB, M - m0);
+  if constexpr (WB) {
+    if (hist0)
+      for (int i = tid; i < MB * kSelectHistBins; i += kGemvThreads) hh[i] = 0u;
+  }
   constexpr int kRows = 8;  // rows per batch and warp (loads in flight)
   {
     const int64_t pos = row0 + tid;
@@ -252,7 +257,19 @@ local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ 
   if constexpr (WB) {  // the global path: every score to HBM, rows in position order
     for (int i = tid; i < mb * kGemvThreads; i += kGemvThreads) {
       const int mm = i / kGemvThreads, rl = i - mm * kGemvThreads;
-      if (row0 + rl < n) S[(size_t)(m0 + mm) * n + row0 + rl] = sc[mm][rl];
+      if (row0 + rl < n) {
+        const float x = sc[mm][rl];
+        S[(size_t)(m0 + mm) * n + row0 + rl] = x;
+        if (hist0) atomicAdd(&hh[mm * kSelectHistBins + (float_key(x) >> (32 - kSelectHistBits))], 1u);
+      }
+    }
+    if (hist0) {  // this CTA's counts into the rows' first selection histograms
+      cta_sync();
+      for (int i = tid; i < mb * kSelectHistBins; i += kGemvThreads) {
+        const uint32_t c = hh[i];
+        const int mm = i / kSelectHistBins;
+        if (c) atomicAdd(hist0 + (size_t)(m0 + mm) * hist0_stride + (i - mm * kSelectHistBins), (int)c);
+      }
     }
     return;
   }
@@ -327,7 +344,7 @@ cudaError_t launch_gemv_mb(const bf16_t* A, const bf16_t* u, const int32_t* toke
 #define GV(KT)                                                                                \
   return launch_kernel(true, local_topk_gemv_kernel<MB, KT, DB>, grid, dim3(kGemvThreads), 0, s, \
                        A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, ready,  \
-                       (float*)nullptr);
+                       (float*)nullptr, (int*)nullptr, 0);
   if (k_tile <= 1) GV(1);
   if (k_tile <= 2) GV(2);
   if (k_tile <= 4) GV(4);
@@ -348,16 +365,17 @@ bool gemv_enabled() {
 }  // namespace
 
 cudaError_t launch_scores_gemv(const bf16_t* A, const bf16_t* u, int64_t n, int r, int M, float* S,
-                               cudaStream_t s) {
+                               cudaStream_t s, int* hist0, int hist0_stride) {
   if (!local_topk_gemv_supported(M, r, kGemvThreads, 1)) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)((n + kGemvThreads - 1) / kGemvThreads), 1);
   if (M <= 1)
     return launch_kernel(true, local_topk_gemv_kernel<1, 1, false, true>, grid, dim3(kGemvThreads),
                          0, s, A, u, (const int32_t*)nullptr, n, r, M, kGemvThreads, 1, 0,
-                         (int32_t*)nullptr, (float*)nullptr, (int*)nullptr, S);
+                         (int32_t*)nullptr, (float*)nullptr, (int*)nullptr, S, hist0,
+                         hist0_stride);
   return launch_kernel(true, local_topk_gemv_kernel<2, 1, true, true>, grid, dim3(kGemvThreads), 0,
                        s, A, u, (const int32_t*)nullptr, n, r, M, kGemvThreads, 1, 0,
-                       (int32_t*)nullptr, (float*)nullptr, (int*)nullptr, S);
+                       (int32_t*)nullptr, (float*)nullptr, (int*)nullptr, S, hist0, hist0_stride);
 }
 
 bool local_topk_gemv_supported(int M, int r, int T, int k_tile) {

@@ -179,37 +179,45 @@ segment_topk_kernel(const float* __restrict__ S, const int32_t* __restrict__ tok
 // ---------------------------------------------------------------- long rows, few rows
 // Global Top-k of rows too long for one CTA to sweep quickly (one CTA per row
 // does every radix pass over the whole row: ~100 us at n = 128256). Here G
-// CTAs share a row. Pass kernels (kMsPasses launches, 12-bit digits from the
-// top of the key): each CTA histograms the keys of its segment that lie in
-// the row's current range [lo, hi] and adds the histogram into the row's
-// global one; the last CTA of the row to finish (atomic ticket, no waiting)
-// finds the boundary digit, narrows [lo, hi], counts the keys above it and
-// marks the row done once the range holds at most kMsDone keys (fp32 scores
-// need two passes in practice: the first 12-bit digit is a sign, the
-// exponent and three mantissa bits). Collection kernel: every CTA appends its keys above
-// the range and inside it to two per-row lists; the last CTA sorts the
-// survivors (at most k + kCap keys) and writes the row's Top-k, score
-// descending, ties by the smaller vocabulary id (the keys are unique). A row
-// the passes left unfinished (more than kCap keys sharing 24 key bits) is
-// finished by the collection kernel's last CTA alone, with the remaining
-// passes over the whole row.
+// CTAs share a row, and no CTA waits on another. Histogram p (p = 0 .. kMsPasses-1)
+// counts the row's keys inside the range left by histograms 0 .. p-1 by
+// their 12-bit digit p from the top of the key; each CTA adds its segment's
+// counts into the row's global histogram. The kernel after it (the next pass,
+// or the collection) derives the narrowed range itself in every CTA, from
+// the finished histogram: the bin holding the k-th largest key, the keys above
+// it, and whether the bin holds at most kMsDone keys (then no further
+// histogram is needed). The first histogram may come from the score
+// writeback (it needs only the score's top 12 bits); fp32 scores need two in
+// practice (the first digit is a sign, the exponent and three mantissa bits).
+// Collection kernel: every CTA appends its keys above the range and inside it
+// to two per-row lists; the last CTA (atomic ticket) sorts both lists (the
+// ones above first, all of them; the ones inside to complete k) and writes
+// the row's Top-k, score descending, ties by the smaller vocabulary id (the
+// keys are unique). A row whose range still holds more than kCap keys after
+// the last histogram is finished by the collection kernel's last CTA alone,
+// with the remaining passes over the whole row.
 constexpr int kMsThreads = 1024;
-constexpr int kMsPasses = 2;      // launched passes; later digits in the fallback
-constexpr int kMsStateInts = 16;  // per-row state, then the row's kBins histogram
-// A row is done once its boundary range holds at most this many keys: the
-// collection's last CTA then sorts about C + kMsDone keys, not C + kCap (the
-// first digit of fp32 scores often leaves a few thousand keys in range).
+constexpr int kMsPasses = 2;      // histograms; later digits in the fallback
+constexpr int kMsStateInts = 32;  // per-row ranges and counters, then the histograms
+constexpr int kMsRowInts = kMsStateInts + kMsPasses * kBins;
+// A range of at most this many keys needs no further histogram: the last
+// CTA of the collection then sorts about k + kMsDone keys.
 constexpr int kMsDone = 512;
+static_assert(kBins == 1 << kSelectHistBits && kDigit == kSelectHistBits, "digit width");
 
-struct MsState {
-  unsigned long long lo, hi;  // current key range (meaningful once pass > 0)
-  int gt;                     // keys above hi
-  int done;                   // the range holds <= kCap keys
-  int ticket;                 // CTAs of the row finished with the current kernel
-  int pass;                   // passes completed
-  int n_sel, n_cand;          // collection counters
+struct MsRange {
+  unsigned long long lo, hi;  // keys in [lo, hi] are still undecided
+  int gt;                     // keys above hi (all selected)
+  int count;                  // keys in [lo, hi]
+  int done;                   // no further histogram
+  int pad;
 };
-static_assert(sizeof(MsState) <= kMsStateInts * sizeof(int), "state slot");
+
+struct MsRow {
+  MsRange range[kMsPasses];  // range[p]: what histogram p counts (p >= 1; 0 is the whole row)
+  int n_sel, n_cand;         // collection list lengths
+};
+static_assert(sizeof(MsRow) <= kMsStateInts * sizeof(int), "row state");
 
 struct MsBoundary {
   unsigned long long lo, hi;
@@ -267,93 +275,132 @@ __device__ void ms_boundary(const uint32_t* hist, uint32_t* part, uint32_t need,
   cta_sync();
 }
 
-// grid (G, M). `zero`: M x (kMsStateInts + kBins) ints, zero before the
-// first pass of a call.
+__device__ __forceinline__ MsRange ms_load_range(const MsRange* r) {
+  MsRange x;
+  x.lo = __ldcg(&r->lo);
+  x.hi = __ldcg(&r->hi);
+  x.gt = __ldcg(&r->gt);
+  x.count = __ldcg(&r->count);
+  x.done = __ldcg(&r->done);
+  x.pad = 0;
+  return x;
+}
+
+// Every thread of the CTA, after the kernel that finished histogram p - 1
+// (p >= 1): the range left by histograms 0 .. p - 1. hist, part: shared
+// scratch (kBins and kMsThreads words).
+__device__ MsRange ms_range(const MsRow* row, const uint32_t* H, int p, int64_t n, int kk,
+                            uint32_t* hist, uint32_t* part, MsBoundary* bnd) {
+  MsRange prev;
+  if (p == 1) {
+    prev.lo = 0ull;
+    prev.hi = ~0ull;
+    prev.gt = 0;
+    prev.count = (int)n;
+    prev.done = 0;
+    prev.pad = 0;
+  } else {
+    prev = ms_load_range(&row->range[p - 1]);
+  }
+  if (prev.done) return prev;
+  const uint32_t* h = H + (size_t)(p - 1) * kBins;
+  for (int i = threadIdx.x; i < kBins; i += kMsThreads) hist[i] = __ldcg(h + i);
+  cta_sync();
+  const int shift = ms_shift(p - 1);
+  ms_boundary(hist, part, (uint32_t)(kk - prev.gt), shift, prev.lo, bnd);
+  MsRange cur;
+  cur.lo = bnd->lo;
+  cur.hi = bnd->hi;
+  cur.gt = prev.gt + bnd->above;
+  cur.count = bnd->count;
+  cur.done = (bnd->count <= kMsDone || shift == 0) ? 1 : 0;
+  cur.pad = 0;
+  return cur;
+}
+
+// grid (G, M), pass p < kMsPasses. `zero`: M x kMsRowInts ints, zero before
+// the first histogram of a call. Histogram p of the keys in the range left by
+// histograms 0 .. p - 1 (all of them for p = 0).
 __global__ void __launch_bounds__(kMsThreads)
 ms_pass_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_ids, int64_t n,
-               int k, int* __restrict__ zero) {
+               int k, int* __restrict__ zero, int p) {
   __shared__ uint32_t hist[kBins];
   __shared__ uint32_t part[kMsThreads];
   __shared__ MsBoundary bnd;
-  __shared__ int s_last;
   const int tid = threadIdx.x, G = gridDim.x, m = blockIdx.y;
-  int* zr = zero + (size_t)m * (kMsStateInts + kBins);
-  MsState* st = reinterpret_cast<MsState*>(zr);
-  uint32_t* ghist = reinterpret_cast<uint32_t*>(zr + kMsStateInts);
-  pdl_wait();  // scores, and the state the previous pass left
-  pdl_trigger();
-  if (*reinterpret_cast<volatile int*>(&st->done)) return;
-  const int pass = st->pass;
-  const uint64_t lo = pass ? st->lo : 0ull, hi = pass ? st->hi : ~0ull;
-  const int gt = st->gt;
-  const int shift = ms_shift(pass);
+  int* zr = zero + (size_t)m * kMsRowInts;
+  MsRow* row_state = reinterpret_cast<MsRow*>(zr);
+  uint32_t* H = reinterpret_cast<uint32_t*>(zr + kMsStateInts);
+  const int kk = (int)min((int64_t)k, n);
   const int64_t per = ms_seg(n, G);
   const int64_t p0 = (int64_t)blockIdx.x * per, p1 = min(n, p0 + per);
   const float* row = S + (size_t)m * n;
+  pdl_wait();  // scores, and the histogram the previous pass left
+  pdl_trigger();
+  // the first two keys are requested while the range is derived
+  const int64_t pa = p0 + tid, pb = pa + kMsThreads;
+  const uint64_t ka = pa < p1 ? key_at(row, token_ids, pa) : 0ull;
+  const uint64_t kb = pb < p1 ? key_at(row, token_ids, pb) : 0ull;
+  uint64_t lo = 0ull, hi = ~0ull;
+  if (p > 0) {
+    const MsRange cur = ms_range(row_state, H, p, n, kk, hist, part, &bnd);
+    if (blockIdx.x == 0 && tid == 0) row_state->range[p] = cur;
+    if (cur.done) return;
+    lo = cur.lo;
+    hi = cur.hi;
+  }
+  const int shift = ms_shift(p);
   for (int i = tid; i < kBins; i += kMsThreads) hist[i] = 0;
   cta_sync();
-  for (int64_t p = p0 + tid; p < p1; p += kMsThreads) {
-    const uint64_t key = key_at(row, token_ids, p);
+  if (pa < p1 && ka >= lo && ka <= hi) atomicAdd(&hist[(ka >> shift) & (kBins - 1)], 1u);
+  if (pb < p1 && kb >= lo && kb <= hi) atomicAdd(&hist[(kb >> shift) & (kBins - 1)], 1u);
+  for (int64_t q = pb + kMsThreads; q < p1; q += kMsThreads) {
+    const uint64_t key = key_at(row, token_ids, q);
     if (key >= lo && key <= hi) atomicAdd(&hist[(key >> shift) & (kBins - 1)], 1u);
   }
   cta_sync();
+  uint32_t* Hp = H + (size_t)p * kBins;
   for (int i = tid; i < kBins; i += kMsThreads)
-    if (hist[i]) atomicAdd(&ghist[i], hist[i]);
-  __threadfence();
-  cta_sync();
-  if (tid == 0) s_last = atomicAdd(&st->ticket, 1) == G - 1;
-  cta_sync();
-  if (!s_last) return;
-  // the last CTA of the row: the row's histogram is complete
-  __threadfence();
-  for (int i = tid; i < kBins; i += kMsThreads) {
-    hist[i] = __ldcg(ghist + i);
-    ghist[i] = 0;  // ready for the next pass
-  }
-  cta_sync();
-  ms_boundary(hist, part, (uint32_t)(min((int64_t)k, n) - gt), shift, lo, &bnd);
-  if (tid == 0) {
-    st->lo = bnd.lo;
-    st->hi = bnd.hi;
-    st->gt = gt + bnd.above;
-    st->done = (bnd.count <= kMsDone || shift == 0) ? 1 : 0;
-    st->pass = pass + 1;
-    st->ticket = 0;
-  }
+    if (hist[i]) atomicAdd(&Hp[i], hist[i]);
 }
 
-// grid (G, M); dynamic shared memory: the last CTA's sort buffer (2 kCap
-// keys), then a histogram and scan space for the fallback passes.
+// grid (G, M); dynamic shared memory: 2 kCap keys of list space, then kBins
+// + kMsThreads words of histogram and scan space. Appends the row's keys above
+// the final range to its `sel` list and those inside it to its `cand` list;
+// ms_rank_kernel orders them.
 __global__ void __launch_bounds__(kMsThreads)
 ms_collect_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_ids, int64_t n,
                   int k, int* __restrict__ zero, uint64_t* __restrict__ sel,
-                  uint64_t* __restrict__ cand, int32_t* __restrict__ out_ids,
-                  float* __restrict__ out_scores) {
+                  uint64_t* __restrict__ cand) {
   extern __shared__ uint64_t keys[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(keys + 2 * kCap);
   uint32_t* part = hist + kBins;
   __shared__ MsBoundary bnd;
-  __shared__ int s_last, s_sel, s_cand, s_base_sel, s_base_cand;
+  __shared__ int s_sel, s_cand, s_base_sel, s_base_cand;
   const int tid = threadIdx.x, G = gridDim.x, m = blockIdx.y;
-  MsState* st = reinterpret_cast<MsState*>(zero + (size_t)m * (kMsStateInts + kBins));
-  pdl_wait();
-  pdl_trigger();
-  const bool done = st->done != 0;
-  uint64_t lo = st->lo, hi = st->hi;
+  int* zr = zero + (size_t)m * kMsRowInts;
+  MsRow* st = reinterpret_cast<MsRow*>(zr);
+  const uint32_t* H = reinterpret_cast<const uint32_t*>(zr + kMsStateInts);
   const int kk = (int)min((int64_t)k, n);
   uint64_t* rsel = sel + (size_t)m * k;
   uint64_t* rcand = cand + (size_t)m * kCap;
   const float* row = S + (size_t)m * n;
-  if (done) {
+  const int64_t per = ms_seg(n, G);
+  const int64_t p0 = (int64_t)blockIdx.x * per, p1 = min(n, p0 + per);
+  if (tid == 0) { s_sel = 0; s_cand = 0; }
+  pdl_wait();
+  pdl_trigger();
+  // the first two keys are requested while the range is derived
+  const int64_t pa = p0 + tid, pb = pa + kMsThreads;
+  const uint64_t ka = pa < p1 ? key_at(row, token_ids, pa) : 0ull;
+  const uint64_t kb = pb < p1 ? key_at(row, token_ids, pb) : 0ull;
+  const MsRange cur = ms_range(st, H, kMsPasses, n, kk, hist, part, &bnd);
+  uint64_t lo = cur.lo, hi = cur.hi;
+  if (cur.count <= kCap) {
     // this CTA's keys above the range and inside it go to shared memory first
     // (at most kk and kCap: the row's lists are no longer), then to the row's
     // lists through one global reservation per list
-    if (tid == 0) { s_sel = 0; s_cand = 0; }
-    cta_sync();
-    const int64_t per = ms_seg(n, G);
-    const int64_t p0 = (int64_t)blockIdx.x * per, p1 = min(n, p0 + per);
-    for (int64_t p = p0 + tid; p < p1; p += kMsThreads) {
-      const uint64_t key = key_at(row, token_ids, p);
+    auto keep = [&](uint64_t key) {
       if (key > hi) {
         const int i = atomicAdd(&s_sel, 1);
         if (i < kCap) keys[i] = key;
@@ -361,7 +408,10 @@ ms_collect_kernel(const float* __restrict__ S, const int32_t* __restrict__ token
         const int i = atomicAdd(&s_cand, 1);
         if (i < kCap) keys[kCap + i] = key;
       }
-    }
+    };
+    if (pa < p1) keep(ka);
+    if (pb < p1) keep(kb);
+    for (int64_t q = pb + kMsThreads; q < p1; q += kMsThreads) keep(key_at(row, token_ids, q));
     cta_sync();
     const int ls = min(s_sel, kCap), lc = min(s_cand, kCap);
     if (tid == 0) {
@@ -373,78 +423,101 @@ ms_collect_kernel(const float* __restrict__ S, const int32_t* __restrict__ token
       if (s_base_sel + i < kk) rsel[s_base_sel + i] = keys[i];
     for (int i = tid; i < lc; i += kMsThreads)
       if (s_base_cand + i < kCap) rcand[s_base_cand + i] = keys[kCap + i];
-    __threadfence();
+    return;
+  }
+  // fallback (more than kCap keys share the histograms' 24 key bits): the
+  // remaining passes over the whole row by the row's first CTA alone
+  if (blockIdx.x != 0) return;
+  int gt = cur.gt;
+  for (int pass = kMsPasses;; ++pass) {
+    const int shift = ms_shift(pass);
+    for (int i = tid; i < kBins; i += kMsThreads) hist[i] = 0;
+    cta_sync();
+    for (int64_t q = tid; q < n; q += kMsThreads) {
+      const uint64_t key = key_at(row, token_ids, q);
+      if (key >= lo && key <= hi) atomicAdd(&hist[(key >> shift) & (kBins - 1)], 1u);
+    }
+    cta_sync();
+    ms_boundary(hist, part, (uint32_t)(kk - gt), shift, lo, &bnd);
+    lo = bnd.lo;
+    hi = bnd.hi;
+    gt += bnd.above;
+    const int count = bnd.count;
+    cta_sync();
+    if (count <= kCap || shift == 0) break;
   }
   cta_sync();
-  if (tid == 0) s_last = atomicAdd(&st->ticket, 1) == G - 1;
-  cta_sync();
-  if (!s_last) return;
-  __threadfence();
-  int ns, nc;
-  if (done) {
-    ns = min(__ldcg(&st->n_sel), kk);
-    nc = min(__ldcg(&st->n_cand), kCap);
-    const int P = pow2_at_least(ns + nc);
-    for (int i = tid; i < P; i += kMsThreads)
-      keys[i] = i < ns ? __ldcg(rsel + i) : (i < ns + nc ? __ldcg(rcand + i - ns) : 0ull);
-  } else {
-    // fallback: the remaining passes over the whole row by this CTA alone
-    int gt = st->gt;
-    for (int pass = st->pass;; ++pass) {
-      const int shift = ms_shift(pass);
-      for (int i = tid; i < kBins; i += kMsThreads) hist[i] = 0;
-      cta_sync();
-      for (int64_t p = tid; p < n; p += kMsThreads) {
-        const uint64_t key = key_at(row, token_ids, p);
-        if (key >= lo && key <= hi) atomicAdd(&hist[(key >> shift) & (kBins - 1)], 1u);
-      }
-      cta_sync();
-      ms_boundary(hist, part, (uint32_t)(kk - gt), shift, lo, &bnd);
-      lo = bnd.lo;
-      hi = bnd.hi;
-      gt += bnd.above;
-      const int count = bnd.count;
-      cta_sync();
-      if (count <= kCap || shift == 0) break;
+  for (int64_t q = tid; q < n; q += kMsThreads) {
+    const uint64_t key = key_at(row, token_ids, q);
+    if (key > hi) {
+      const int i = atomicAdd(&s_sel, 1);
+      if (i < kk) rsel[i] = key;
+    } else if (key >= lo) {
+      const int i = atomicAdd(&s_cand, 1);
+      if (i < kCap) rcand[i] = key;
     }
-    if (tid == 0) { s_sel = 0; s_cand = 0; }
-    cta_sync();
-    for (int64_t p = tid; p < n; p += kMsThreads) {
-      const uint64_t key = key_at(row, token_ids, p);
-      if (key > hi) {
-        const int i = atomicAdd(&s_sel, 1);
-        if (i < kk) keys[i] = key;
-      } else if (key >= lo) {
-        const int i = atomicAdd(&s_cand, 1);
-        if (i < kCap) keys[kCap + i] = key;
-      }
-    }
-    cta_sync();
-    ns = min(s_sel, kk);
-    nc = min(s_cand, kCap);
-    // move the candidates next to the selected keys (read all, then write)
-    uint64_t mv[kCap / kMsThreads];
-#pragma unroll
-    for (int r = 0; r < kCap / kMsThreads; ++r) {
-      const int i = tid + r * kMsThreads;
-      mv[r] = i < nc ? keys[kCap + i] : 0ull;
-    }
-    cta_sync();
-#pragma unroll
-    for (int r = 0; r < kCap / kMsThreads; ++r) {
-      const int i = tid + r * kMsThreads;
-      if (i < nc) keys[ns + i] = mv[r];
-    }
-    const int P = pow2_at_least(ns + nc);
-    for (int i = ns + nc + tid; i < P; i += kMsThreads) keys[i] = 0ull;
   }
   cta_sync();
-  const int P = pow2_at_least(ns + nc);
-  bitonic_desc(keys, P);
-  const int take = min(kk, ns + nc);
-  for (int j = tid; j < take; j += kMsThreads) {
-    out_ids[(size_t)m * k + j] = key_id(keys[j]);
-    if (out_scores) out_scores[(size_t)m * k + j] = key_score(keys[j]);
+  if (tid == 0) {
+    st->n_sel = min(s_sel, kk);
+    st->n_cand = min(s_cand, kCap);
+  }
+}
+
+// Output order of the collected keys. Every key above the range outranks
+// every key inside it, so a key's place is the number of keys of its own list
+// above it, plus the length of the `sel` list for a `cand` key; places below
+// k are written. The keys are unique, so the places are too. grid (X, M); the
+// lists' keys in chunks of 32, `sel` chunks first (its length rounded up to
+// 32), chunk c taken by CTA c mod X. Each warp counts over one eighth of the
+// chunk's list (in shared memory) for the chunk's 32 keys, one per lane.
+constexpr int kRankThreads = 256;
+constexpr int kRankWarps = kRankThreads / 32;
+
+__global__ void __launch_bounds__(kRankThreads)
+ms_rank_kernel(int64_t n, int k, const int* __restrict__ zero, const uint64_t* __restrict__ sel,
+               const uint64_t* __restrict__ cand, int32_t* __restrict__ out_ids,
+               float* __restrict__ out_scores) {
+  __shared__ uint64_t list[kCap];
+  __shared__ uint32_t cnt[kRankWarps][32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, m = blockIdx.y;
+  const MsRow* st = reinterpret_cast<const MsRow*>(zero + (size_t)m * kMsRowInts);
+  const int kk = (int)min((int64_t)k, n);
+  pdl_wait();
+  pdl_trigger();
+  const int ns = min(__ldcg(&st->n_sel), kk), nc = min(__ldcg(&st->n_cand), kCap);
+  const int s0 = (ns + 31) & ~31;
+  const int chunks = s0 / 32 + (nc + 31) / 32;
+  int loaded = -1;  // which list is in shared memory: 0 sel, 1 cand
+  for (int c = blockIdx.x; c < chunks; c += gridDim.x) {
+    const int which = 32 * c < s0 ? 0 : 1;
+    const int len = which ? nc : ns;
+    if (which != loaded) {
+      const uint64_t* src = which ? cand + (size_t)m * kCap : sel + (size_t)m * k;
+      cta_sync();  // the previous chunk is done with the list
+      for (int i = tid; i < len; i += kRankThreads) list[i] = __ldcg(src + i);
+      cta_sync();
+      loaded = which;
+    }
+    const int idx = 32 * c - (which ? s0 : 0) + lane;
+    const uint64_t x = idx < len ? list[idx] : ~0ull;
+    const int per = (len + kRankWarps - 1) / kRankWarps;
+    const int j0 = warp * per, j1 = min(len, j0 + per);
+    uint32_t above = 0;
+#pragma unroll 4
+    for (int j = j0; j < j1; ++j) above += list[j] > x ? 1u : 0u;
+    cnt[warp][lane] = above;
+    cta_sync();
+    if (warp == 0 && idx < len) {
+      uint32_t place = which ? (uint32_t)ns : 0u;
+#pragma unroll
+      for (int w = 0; w < kRankWarps; ++w) place += cnt[w][lane];
+      if (place < (uint32_t)kk) {
+        out_ids[(size_t)m * k + place] = key_id(x);
+        if (out_scores) out_scores[(size_t)m * k + place] = key_score(x);
+      }
+    }
+    cta_sync();  // cnt is reused
   }
 }
 
@@ -460,7 +533,9 @@ bool row_select_multi(int64_t n, int M, int k) {
   return n > 2 * kCap && k <= kCap && M <= 2 * 152;
 }
 
-int row_select_multi_ints(int M) { return M * (kMsStateInts + kBins); }
+int row_select_multi_ints(int M) { return M * kMsRowInts; }
+
+int row_select_multi_hist0(int m) { return m * kMsRowInts + kMsStateInts; }
 
 size_t row_select_multi_bytes(int M, int k) {
   return (size_t)M * ((size_t)k + kCap) * sizeof(uint64_t);
@@ -468,24 +543,32 @@ size_t row_select_multi_bytes(int M, int k) {
 
 cudaError_t launch_row_select_multi(const float* S, const int32_t* token_ids, int64_t n, int M,
                                     int k, int32_t* out_ids, float* out_scores, int* zero,
-                                    void* scratch, cudaStream_t s) {
+                                    void* scratch, bool hist0_filled, cudaStream_t s) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const dim3 grid((unsigned)ms_ctas(n, M, sms), (unsigned)M);
-  for (int pass = 0; pass < kMsPasses; ++pass) {
+  for (int pass = hist0_filled ? 1 : 0; pass < kMsPasses; ++pass) {
     cudaError_t e = launch_kernel(true, ms_pass_kernel, grid, dim3(kMsThreads), 0, s, S, token_ids,
-                                  n, k, zero);
+                                  n, k, zero, pass);
     if (e != cudaSuccess) return e;
   }
   uint64_t* sel = static_cast<uint64_t*>(scratch);
   uint64_t* cand = sel + (size_t)M * k;
-  // k + kCap <= 2 kCap keys, then the fallback's histogram and scan space
+  // 2 kCap keys of list space, then the histogram and scan space
   const size_t smem = (size_t)2 * kCap * sizeof(uint64_t) + (kBins + kMsThreads) * sizeof(uint32_t);
   static int smem_set[64] = {0};
   cudaError_t e = ensure_dynamic_smem(ms_collect_kernel, smem, smem_set);
   if (e != cudaSuccess) return e;
-  return launch_kernel(true, ms_collect_kernel, grid, dim3(kMsThreads), smem, s, S, token_ids, n, k,
-                       zero, sel, cand, out_ids, out_scores);
+  e = launch_kernel(true, ms_collect_kernel, grid, dim3(kMsThreads), smem, s, S, token_ids, n, k,
+                    zero, sel, cand);
+  if (e != cudaSuccess) return e;
+  // one CTA per chunk of 32 of the usual lists (k + kMsDone keys); longer
+  // candidate lists are taken in turns
+  const int kk = (int)(k < n ? k : n);
+  const dim3 rgrid((unsigned)((kk + 31) / 32 + (kMsDone + 31) / 32), (unsigned)M);
+  return launch_kernel(true, ms_rank_kernel, rgrid, dim3(kRankThreads), 0, s, n, k,
+                       (const int*)zero, (const uint64_t*)sel, (const uint64_t*)cand, out_ids,
+                       out_scores);
 }
 
 cudaError_t launch_segment_topk(const float* S, const int32_t* token_ids, int64_t n, int M,
