@@ -204,6 +204,11 @@ constexpr int kMsRowInts = kMsStateInts + kMsPasses * kBins;
 // CTA of the collection then sorts about k + kMsDone keys.
 constexpr int kMsDone = 512;
 static_assert(kBins == 1 << kSelectHistBits && kDigit == kSelectHistBits, "digit width");
+// The histograms' digits lie in the score's order bits (the key's top 32), so
+// the passes read only scores, and a range they leave decides every key by
+// its score bits alone (its low 32 bits are all free): the collection reads
+// a vocabulary id only for the keys it keeps.
+static_assert(64 - kDigit * kMsPasses >= 32, "histogram digits inside the score bits");
 
 struct MsRange {
   unsigned long long lo, hi;  // keys in [lo, hi] are still undecided
@@ -226,6 +231,50 @@ struct MsBoundary {
 
 __device__ __forceinline__ int64_t ms_seg(int64_t n, int G) { return (n + G - 1) / G; }
 __device__ __forceinline__ int ms_shift(int pass) { return max(0, 64 - kDigit * (pass + 1)); }
+
+// A CTA's scan of the scores of positions [p0, p1) of one row (row = S + off,
+// off = m * n floats from a 16-byte aligned S): 16-byte loads of four scores
+// over the aligned middle, one score each for the at most three positions
+// before and after it. start() requests the thread's first four scores (so
+// they travel while the caller does other work); run() calls f(score, position)
+// for every score of the thread, in no particular order.
+struct MsScan {
+  int64_t p0, p1, pa, nb;
+  float4 pre;
+
+  __device__ __forceinline__ void start(const float* row, int64_t off, int64_t p0_, int64_t p1_) {
+    p0 = p0_;
+    p1 = p1_;
+    pa = min(p1, p0 + ((4 - ((off + p0) & 3)) & 3));
+    nb = (p1 - pa) >> 2;
+    pre = (int64_t)threadIdx.x < nb ? __ldcg(reinterpret_cast<const float4*>(row + pa) + threadIdx.x)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
+  template <typename F>
+  __device__ __forceinline__ void run(const float* row, F&& f) const {
+    const int tid = threadIdx.x;
+    const int64_t pe = pa + nb * 4;
+    if (tid < pa - p0) f(__ldcg(row + p0 + tid), p0 + tid);
+    if (tid < p1 - pe) f(__ldcg(row + pe + tid), pe + tid);
+    const float4* v = reinterpret_cast<const float4*>(row + pa);
+    auto four = [&](const float4& a, int64_t i) {
+      const int64_t q = pa + 4 * i;
+      f(a.x, q);
+      f(a.y, q + 1);
+      f(a.z, q + 2);
+      f(a.w, q + 3);
+    };
+    if (tid < nb) four(pre, tid);
+    int64_t i = tid + kMsThreads;
+    for (; i + kMsThreads < nb; i += 2 * kMsThreads) {  // two vectors in flight
+      const float4 a = __ldcg(v + i), b = __ldcg(v + i + kMsThreads);
+      four(a, i);
+      four(b, i + kMsThreads);
+    }
+    if (i < nb) four(__ldcg(v + i), i);
+  }
+};
 
 // Every thread of the CTA (kMsThreads): with hist[] the kBins counts of the
 // keys in [lo, hi] by the digit at `shift`, find the bin holding the need-th
@@ -321,7 +370,7 @@ __device__ MsRange ms_range(const MsRow* row, const uint32_t* H, int p, int64_t 
 // grid (G, M), pass p < kMsPasses. `zero`: M x kMsRowInts ints, zero before
 // the first histogram of a call. Histogram p of the keys in the range left by
 // histograms 0 .. p - 1 (all of them for p = 0).
-__global__ void __launch_bounds__(kMsThreads)
+__global__ void __launch_bounds__(kMsThreads, 2)
 ms_pass_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_ids, int64_t n,
                int k, int* __restrict__ zero, int p) {
   __shared__ uint32_t hist[kBins];
@@ -337,27 +386,23 @@ ms_pass_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_id
   const float* row = S + (size_t)m * n;
   pdl_wait();  // scores, and the histogram the previous pass left
   pdl_trigger();
-  // the first two keys are requested while the range is derived
-  const int64_t pa = p0 + tid, pb = pa + kMsThreads;
-  const uint64_t ka = pa < p1 ? key_at(row, token_ids, pa) : 0ull;
-  const uint64_t kb = pb < p1 ? key_at(row, token_ids, pb) : 0ull;
-  uint64_t lo = 0ull, hi = ~0ull;
+  MsScan scan;
+  scan.start(row, (int64_t)m * n, p0, p1);  // in flight while the range is derived
+  uint32_t lo = 0u, hi = 0xFFFFFFFFu;  // the range's score bits
   if (p > 0) {
     const MsRange cur = ms_range(row_state, H, p, n, kk, hist, part, &bnd);
     if (blockIdx.x == 0 && tid == 0) row_state->range[p] = cur;
     if (cur.done) return;
-    lo = cur.lo;
-    hi = cur.hi;
+    lo = (uint32_t)(cur.lo >> 32);
+    hi = (uint32_t)(cur.hi >> 32);
   }
-  const int shift = ms_shift(p);
+  const int shift = ms_shift(p) - 32;
   for (int i = tid; i < kBins; i += kMsThreads) hist[i] = 0;
   cta_sync();
-  if (pa < p1 && ka >= lo && ka <= hi) atomicAdd(&hist[(ka >> shift) & (kBins - 1)], 1u);
-  if (pb < p1 && kb >= lo && kb <= hi) atomicAdd(&hist[(kb >> shift) & (kBins - 1)], 1u);
-  for (int64_t q = pb + kMsThreads; q < p1; q += kMsThreads) {
-    const uint64_t key = key_at(row, token_ids, q);
+  scan.run(row, [&](float x, int64_t) {
+    const uint32_t key = float_key(x);
     if (key >= lo && key <= hi) atomicAdd(&hist[(key >> shift) & (kBins - 1)], 1u);
-  }
+  });
   cta_sync();
   uint32_t* Hp = H + (size_t)p * kBins;
   for (int i = tid; i < kBins; i += kMsThreads)
@@ -368,7 +413,7 @@ ms_pass_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_id
 // + kMsThreads words of histogram and scan space. Appends the row's keys above
 // the final range to its `sel` list and those inside it to its `cand` list;
 // ms_rank_kernel orders them.
-__global__ void __launch_bounds__(kMsThreads)
+__global__ void __launch_bounds__(kMsThreads, 2)
 ms_collect_kernel(const float* __restrict__ S, const int32_t* __restrict__ token_ids, int64_t n,
                   int k, int* __restrict__ zero, uint64_t* __restrict__ sel,
                   uint64_t* __restrict__ cand) {
@@ -390,28 +435,30 @@ ms_collect_kernel(const float* __restrict__ S, const int32_t* __restrict__ token
   if (tid == 0) { s_sel = 0; s_cand = 0; }
   pdl_wait();
   pdl_trigger();
-  // the first two keys are requested while the range is derived
-  const int64_t pa = p0 + tid, pb = pa + kMsThreads;
-  const uint64_t ka = pa < p1 ? key_at(row, token_ids, pa) : 0ull;
-  const uint64_t kb = pb < p1 ? key_at(row, token_ids, pb) : 0ull;
+  MsScan scan;
+  scan.start(row, (int64_t)m * n, p0, p1);  // in flight while the range is derived
   const MsRange cur = ms_range(st, H, kMsPasses, n, kk, hist, part, &bnd);
   uint64_t lo = cur.lo, hi = cur.hi;
   if (cur.count <= kCap) {
     // this CTA's keys above the range and inside it go to shared memory first
     // (at most kk and kCap: the row's lists are no longer), then to the row's
-    // lists through one global reservation per list
-    auto keep = [&](uint64_t key) {
-      if (key > hi) {
+    // lists through one global reservation per list. The range's low 32 bits
+    // are free, so the score bits decide.
+    const uint32_t lo32 = (uint32_t)(lo >> 32), hi32 = (uint32_t)(hi >> 32);
+    auto keep = [&](float x, int64_t q) {
+      const uint32_t k32 = float_key(x);
+      if (k32 < lo32) return;
+      const int32_t id = token_ids ? __ldg(token_ids + q) : (int32_t)q;
+      const uint64_t key = select_key(x, id);
+      if (k32 > hi32) {
         const int i = atomicAdd(&s_sel, 1);
         if (i < kCap) keys[i] = key;
-      } else if (key >= lo) {
+      } else {
         const int i = atomicAdd(&s_cand, 1);
         if (i < kCap) keys[kCap + i] = key;
       }
     };
-    if (pa < p1) keep(ka);
-    if (pb < p1) keep(kb);
-    for (int64_t q = pb + kMsThreads; q < p1; q += kMsThreads) keep(key_at(row, token_ids, q));
+    scan.run(row, keep);
     cta_sync();
     const int ls = min(s_sel, kCap), lc = min(s_cand, kCap);
     if (tid == 0) {
@@ -521,8 +568,11 @@ ms_rank_kernel(int64_t n, int k, const int* __restrict__ zero, const uint64_t* _
   }
 }
 
+// CTAs per row: one wave in all (two 1024-thread CTAs per SM), so every CTA
+// pays the range derivation and its barriers once, and at least ~2 keys per
+// thread.
 int ms_ctas(int64_t n, int M, int sms) {
-  const int64_t want = (4 * (int64_t)sms + M - 1) / M;
+  const int64_t want = 2 * (int64_t)sms / M;
   const int64_t cap = (n + 2047) / 2048;  // at least ~2 keys per thread
   return (int)max((int64_t)1, min(want, cap));
 }

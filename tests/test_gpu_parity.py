@@ -96,6 +96,45 @@ def test_global_select_all_scores_tied(L, M):
     assert L.last_device_error() == 0
 
 
+@pytest.mark.parametrize("n_tie", [2000, 5000])
+@pytest.mark.parametrize("M", [1, 2, 3])
+def test_global_select_three_score_levels(L, M, n_tie):
+    # every row of A is 2a, a or a/2 for one row a with a.u > 0, and the
+    # hidden rows are h, h/2, 2h: each row's scores are exactly 2s, s and s/2
+    # (power-of-two scaling is exact in bf16 and in the fp32 sums). With 700
+    # rows at 2s and n_tie rows at s, the Top-1024 is the 2s rows by id, then
+    # the 324 smallest ids of the s rows. 2000 tied rows leave the several-CTA
+    # selection's final range with 2000 keys (the ranking takes its chunks in
+    # turns); 5000 are more than its lists hold (one CTA finishes the row). M
+    # <= 2 counts the first histogram in the GEMV score writeback (r = 256),
+    # M = 3 in a pass kernel. n % 4 = 3: rows after the first start off a
+    # 16-byte boundary (the score scans' scalar head and tail).
+    n, d, r, C, n_hi = 20003, 64, 256, 1024, 700
+    g = np.random.default_rng(71)
+    B = synth.bf16_bits_from_f32((g.standard_normal((r, d)) / 8).astype(np.float32))
+    h0 = g.standard_normal(d).astype(np.float32)
+    h = synth.bf16_bits_from_f32(np.stack([h0 * c for c in (1.0, 0.5, 2.0)[:M]]).astype(np.float32))
+    u = O.project_u(O.bf16_bits_to_f64(B), O.bf16_bits_to_f64(h[:1]))[0]
+    a = (np.where(u >= 0, 1.0, -1.0) * (0.5 + g.random(r))).astype(np.float32)
+    a = synth.bf16_bits_to_f32(synth.bf16_bits_from_f32(a))
+    perm = g.permutation(n)
+    A = np.empty((n, r), dtype=np.float32)
+    A[:] = 0.5 * a
+    A[perm[:n_hi]] = 2.0 * a
+    A[perm[n_hi:n_hi + n_tie]] = a
+    tok = g.permutation(n).astype(np.int32)
+    ids, sc = L.lowrank_score_topk(L.GLOBAL, dev_bf16(synth.bf16_bits_from_f32(A)), dev_bf16(B),
+                                   dev_bf16(h), dev_i32(tok), C, with_scores=True)
+    ids, sc = host(ids), host(sc)
+    want = np.concatenate([np.sort(tok[perm[:n_hi]]),
+                           np.sort(tok[perm[n_hi:n_hi + n_tie]])[:C - n_hi]])
+    for m in range(M):
+        assert np.array_equal(ids[m], want), m
+        assert np.all(sc[m, :n_hi] == sc[m, 0]) and np.all(sc[m, n_hi:] == sc[m, n_hi])
+        assert sc[m, n_hi] > 0 and sc[m, 0] == 2 * sc[m, n_hi]
+    assert L.last_device_error() == 0
+
+
 def test_scores_match_oracle(L, small):
     W, A, B, h, tok = _dev(small)
     ids, sc = L.lowrank_score_topk(L.LOCAL, A, B, h, tok, 128, 4, with_scores=True)
