@@ -165,6 +165,25 @@ def test_two_stage(L, mode, C, k, temp):
     P.check_q(host(q), ex, temp)
 
 
+@pytest.mark.parametrize("T,k", [(256, 2), (64, 8), (32, 1)])
+@pytest.mark.parametrize("M", [1, 2])
+def test_two_stage_gemv_scoring(L, M, T, k):
+    # one or two hidden vectors at r = 256 take the CUDA-core scoring kernel
+    # (tiles of 32-256 rows in one 256-row CTA). d = 264: W rows and h end off
+    # a 256-element step; n = 5003: the last tile is partial and the last CTA
+    # holds tile slots past n.
+    case = make_case(5003, 264, 256, M, seed=23, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    ids, lg, q = L.two_stage(L.LOCAL, W, A, B, h, tok, T, k, temperature=0.7)
+    _, S, h64, SL = oracle_scores(case, with_slack=True)
+    ids = host(ids)
+    P.check_ids("local", ids, S, case["tok"], T, k, slack_pos=SL)
+    ex = P.exact_logits(case["W"], h64, ids)
+    P.check_logits(host(lg), ex)
+    P.check_q(host(q), ex, 0.7)
+    assert L.last_device_error() == 0
+
+
 def test_two_stage_identity_token_ids(L):
     case = make_case(1024, 64, 16, 2, seed=14, shuffle=False)
     W, A, B, h, _ = _dev(case)
