@@ -319,6 +319,55 @@ def time_after_q(torch, L, out, hbm, reps=50):
     return res
 
 
+def time_noalloc(torch, L, head, rot_h, hbm, reps=40):
+    """Graph-replayed timings of the no-allocation entry point
+    (lmhead_two_stage_local_noalloc: CUDA-core scoring at every M, softmax
+    inside the gather, scratch in a fixed device array) on the headline head
+    at M = 1 and 64, beside the workspace call's numbers in the sweep."""
+    import ctypes
+    n, d = head["W"].shape
+    r = head["B"].shape[0]
+    lib = L.load()
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    res = []
+    for Mx in (1, 64):
+        hs = [dev(hidden(head["W"], Mx, 0)) for _ in rot_h]
+        K = L.candidate_count(L.LOCAL, n, WORKLOAD.T, WORKLOAD.k_tile)
+        outs = [(torch.empty((Mx, K), dtype=torch.int32, device="cuda"),
+                 torch.empty((Mx, K), dtype=torch.float32, device="cuda"),
+                 torch.empty((Mx, K), dtype=torch.float32, device="cuda")) for _ in rot_h]
+        status = []
+
+        def calls():
+            st = torch.cuda.current_stream().cuda_stream
+            for j, rt in enumerate(rot_h):
+                Wt, At, Bt, tk = rt[0], rt[1], rt[2], rt[3]
+                ids, lg, q = outs[j]
+                status.append(lib.lmhead_two_stage_local_noalloc(
+                    Wt.data_ptr(), At.data_ptr(), Bt.data_ptr(), hs[j].data_ptr(), tk.data_ptr(),
+                    n, d, r, Mx, WORKLOAD.T, WORKLOAD.k_tile, ctypes.c_float(1.0),
+                    ids.data_ptr(), lg.data_ptr(), q.data_ptr(), st))
+
+        gr = make_graph(torch, calls)
+        if any(x != 0 for x in status):
+            raise RuntimeError(f"lmhead_two_stage_local_noalloc returned {status}")
+        gr.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps // len(rot_h)):
+            gr.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps // len(rot_h) * len(rot_h))
+        res.append({"M": Mx, "us": round(us, 2), "vecs_per_s": round(Mx / us * 1e6, 1)})
+        del gr
+    return res
+
+
 def time_cluster(torch, L, head, rot_h, hbm, group=128, G=8, reps=40):
     """Graph-replayed timings of the cluster-level route on the same head (A
     in vocabulary order, groups of `group` consecutive rows, the G best groups
@@ -794,9 +843,11 @@ def run_ours(args):
     # the steps after q (draft selection, chain verification), for context
     after_q = {}
     cluster = []
+    noalloc = []
     if not args.no_sweep and rank == 0:
         after_q = time_after_q(torch, L, outs[0], hbm)
         cluster = time_cluster(torch, L, head, rot, hbm)
+        noalloc = time_noalloc(torch, L, head, rot, hbm)
     configs = []
     if not args.no_configs and rank == 0:
         configs = time_configs(torch, L, hbm)
@@ -825,7 +876,7 @@ def run_ours(args):
             "step_hbm_frac": round(step_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm, 4),
             "unique_rows": U, "latency_us": lat, "parity_counts": parity, "sweep": sweep,
             "configs": configs, "vs_dense": dense_speedups(configs), "after_q": after_q,
-            "cluster_route": cluster,
+            "cluster_route": cluster, "noalloc": noalloc,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
