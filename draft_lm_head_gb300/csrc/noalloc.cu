@@ -5,8 +5,8 @@
 // at start-up and allows no allocation afterwards in its decode loop, or C/C++
 // code that embeds this library without any device allocator of its own. Such
 // callers can still pass inputs and outputs, but not the scratch that
-// lmhead_two_stage takes from its workspace (u, M x r bf16, and the per-row
-// softmax tickets, M ints).
+// lmhead_two_stage takes from its workspace (u, M x r bf16, and the
+// tensor-core scoring kernel's tile counters).
 //
 // Here that scratch is a fixed file-scope device array. Every GPU that loads
 // the library holds it (kScratchBytes) until the process exits. In host code
@@ -16,9 +16,12 @@
 // kernels. The call allocates nothing: no cudaMalloc, no cudaFree, no
 // allocating library routine.
 //
-// All calls share the array and it keeps the last call's contents. The
-// tickets must start at zero; the first kernel of every call zeroes them (u
-// is fully overwritten). Calls whose work overlaps on the GPU (two streams,
+// All calls share the array and it keeps the last call's contents. The tile
+// counters must start at zero; the first kernel of every call zeroes them (u
+// is fully overwritten). Scoring takes the routes lmhead_two_stage takes
+// except where its scratch grows with M and n (tiles that are not a multiple
+// of 128 rows on the tensor cores: partial lists per CTA); those score on the
+// CUDA-core tile kernel. The gather never overlaps the scoring kernel here. Calls whose work overlaps on the GPU (two streams,
 // two host threads) race on the array and corrupt each other's results.
 #include <stdint.h>
 
@@ -33,7 +36,8 @@ constexpr int kNoAllocMaxM = 256;
 constexpr int kNoAllocMaxR = 1024;
 constexpr size_t kUBytes = (size_t)kNoAllocMaxM * kNoAllocMaxR * sizeof(bf16_t);  // 512 KiB
 constexpr size_t kTicketsOffset = kUBytes;                                     // 256-aligned
-constexpr size_t kScratchBytes = kUBytes + (size_t)kNoAllocMaxM * sizeof(int);
+constexpr int kTicketInts = kNoAllocMaxM;  // tile counters (one per 128 hidden vectors)
+constexpr size_t kScratchBytes = kUBytes + (size_t)kTicketInts * sizeof(int);
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -80,11 +84,25 @@ extern "C" int lmhead_two_stage_local_noalloc(
   bf16_t* u = reinterpret_cast<bf16_t*>(scratch);
   int* tickets = reinterpret_cast<int*>(scratch + kTicketsOffset);
   cudaStream_t s = (cudaStream_t)stream;
-  if (launch_project_u(B, h, d, r, M, u, tickets, M, s) != cudaSuccess) return LMHEAD_ERR_CUDA;
-  if (launch_local_topk_fma(A, u, token_ids, n, r, M, T, k_tile, out_ids, nullptr, s) != cudaSuccess)
+  // tensor-core scoring where its scratch is only the tile counters (tiles
+  // of a multiple of 128 rows, more than the GEMV kernel's two vectors)
+  const bool tc = local_topk_tc_supported(r, T, k_tile) && T % 128 == 0 &&
+                  !local_topk_gemv_supported(M, r, T, k_tile);
+  const int counters = tc ? local_topk_tc_tickets(n, M, T) : 0;
+  if (counters > kTicketInts) return LMHEAD_ERR_UNSUPPORTED;
+  if (launch_project_u(B, h, d, r, M, u, counters ? tickets : nullptr, counters, s) != cudaSuccess)
     return LMHEAD_ERR_CUDA;
-  if (launch_gather_logits(W, h, out_ids, n, d, M, (int)K, out_logits, out_q, 1.f / temperature,
-                           tickets, device_error_word(), s) != cudaSuccess)
+  const cudaError_t e =
+      tc ? launch_local_topk_tc(A, u, token_ids, n, r, M, T, k_tile, out_ids, nullptr, nullptr,
+                                tickets, device_error_word(), s)
+         : launch_local_topk_fma(A, u, token_ids, n, r, M, T, k_tile, out_ids, nullptr, s);
+  if (e != cudaSuccess) return LMHEAD_ERR_CUDA;
+  // the candidates in blocks of 16 tiles (all hidden vectors of a block
+  // together, so repeated W rows hit L2), then the softmax launch
+  if (launch_gather_logits(W, h, out_ids, n, d, M, (int)K, out_logits, nullptr, 1.f / temperature,
+                           nullptr, device_error_word(), s, kReadyTiles * k_tile) != cudaSuccess)
+    return LMHEAD_ERR_CUDA;
+  if (launch_row_softmax(out_logits, M, K, 1.f / temperature, out_q, s) != cudaSuccess)
     return LMHEAD_ERR_CUDA;
   return LMHEAD_OK;
 }

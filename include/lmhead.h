@@ -207,15 +207,16 @@ int lmhead_pruned_head(const lmhead_bf16* W_pruned, const lmhead_bf16* h, int n_
  * forbids allocation in its decode loop, or C/C++ code embedding the library
  * with no device allocator of its own. Arguments, outputs and results are
  * those of lmhead_two_stage with mode = LMHEAD_LOCAL, C_or_tile = T.
- *   Speed: it always scores on CUDA cores (the warp-per-row GEMV kernel for
- *   one or two hidden vectors at r = 256, otherwise the CUDA-core tile
- *   kernel), because the tensor-core scoring needs scratch that grows with M
- *   and n. At one or two hidden vectors it runs the same kernels as
- *   lmhead_two_stage; at larger M (the 64-vector batch of the 128256-row head,
- *   say) it is several times slower than lmhead_two_stage.
+ *   Speed: it scores as lmhead_two_stage does (the warp-per-row GEMV kernel
+ *   for one or two hidden vectors at r = 256, the tensor-core kernel for
+ *   tiles of a multiple of 128 rows), except that tiles of other sizes score
+ *   on the CUDA-core tile kernel (the tensor-core form for them needs scratch
+ *   that grows with M and n), and the gather never overlaps the scoring
+ *   kernel, so at 9 to 256 hidden vectors it is somewhat slower than
+ *   lmhead_two_stage.
  *   Scratch: a fixed static device array of 513 KiB (u for M <= 256 and
- *   r <= 1024, plus M per-row counters) held by every GPU that loads the
- *   library until the process exits. M > 256, r > 1024 or k_tile > 32
+ *   r <= 1024, plus the scoring kernel's tile counters) held by every GPU
+ *   that loads the library until the process exits. M > 256, r > 1024 or k_tile > 32
  *   returns LMHEAD_ERR_UNSUPPORTED and enqueues nothing.
  *   Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
