@@ -42,8 +42,11 @@ def _against_oracle(case, rows, T, k, temp, ids, lg, q):
 
 
 @pytest.mark.parametrize("n,d,r,T,k,calls", [
-    # 12 tiles, ragged last tile; 11 and 13 hidden vectors (CUDA-core scoring)
+    # 12 tiles, ragged last tile; 11 and 13 hidden vectors (tensor-core
+    # scoring, its tile counters in the fixed scratch)
     (3000, 128, 32, 256, 2, ((slice(0, 11), 1.0), (slice(11, 24), 0.7))),
+    # 96-row tiles (not a multiple of 128: the CUDA-core tile kernel)
+    (3000, 128, 32, 96, 2, ((slice(0, 5), 1.0), (slice(5, 12), 0.7))),
     # the decode-loop shape: one and two hidden vectors, r = 256, 256-row
     # tiles (the warp-per-row scoring kernel), ragged last tile of 64 rows
     (4160, 256, 256, 256, 2, ((slice(0, 1), 1.0), (slice(1, 3), 0.8))),
