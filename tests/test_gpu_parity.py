@@ -76,6 +76,29 @@ def test_global_select_long_rows(L):
         P.check_ids("global", host(ids), S, case["tok"], C, slack_pos=SL)
 
 
+@pytest.mark.parametrize("M", [1, 2, 16])
+def test_global_select_several_ctas_order(L, M):
+    # the several-CTA selection on random scores (n = 30001: odd rows, off a
+    # 16-byte boundary after the first): ids against the oracle, every row
+    # score-descending with equal scores by ascending id and no id twice.
+    # r = 256: M <= 2 counts the first histogram in the GEMV score writeback;
+    # M = 16 places the keys two to a lane.
+    n, d, r = 30001, 256, 256
+    case = make_case(n, d, r, M, seed=41, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    _, S, _, SL = oracle_scores(case, with_slack=True)
+    for C in (1, 64, 1000, 4096):
+        ids, sc = L.lowrank_score_topk(L.GLOBAL, A, B, h, tok, C, with_scores=True)
+        ids, sc = host(ids), host(sc)
+        P.check_ids("global", ids, S, case["tok"], C, slack_pos=SL)
+        P.check_order("global", ids, sc, C, 0, n)
+        for m in range(M):
+            assert np.unique(ids[m]).size == C, (C, m)
+            tie = sc[m, 1:] == sc[m, :-1]
+            assert np.all(ids[m, 1:][tie] > ids[m, :-1][tie]), (C, m)
+    assert L.last_device_error() == 0
+
+
 @pytest.mark.parametrize("M", [1, 3])
 def test_global_select_all_scores_tied(L, M):
     # every row of A equal: all scores tie, so the Top-C is exactly the C
