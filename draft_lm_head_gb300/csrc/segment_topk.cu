@@ -13,7 +13,8 @@
 // pass one read of the segment, histogram in shared memory) until the
 // boundary digit holds few enough keys for shared memory, then one collection
 // pass and a bitonic sort of the survivors. Short segments (<= 8192 keys):
-// loaded whole and bitonic-sorted.
+// loaded whole and bitonic-sorted. Long rows and few of them (the global
+// Top-C at up to 304 rows) use several CTAs per row instead (below).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -190,18 +191,19 @@ segment_topk_kernel(const float* __restrict__ S, const int32_t* __restrict__ tok
 // writeback (it needs only the score's top 12 bits); fp32 scores need two in
 // practice (the first digit is a sign, the exponent and three mantissa bits).
 // Collection kernel: every CTA appends its keys above the range and inside it
-// to two per-row lists; the last CTA (atomic ticket) sorts both lists (the
-// ones above first, all of them; the ones inside to complete k) and writes
-// the row's Top-k, score descending, ties by the smaller vocabulary id (the
-// keys are unique). A row whose range still holds more than kCap keys after
-// the last histogram is finished by the collection kernel's last CTA alone,
-// with the remaining passes over the whole row.
+// to two per-row lists. Rank kernel: every kept key's place in the row's
+// Top-k (score descending, ties by the smaller vocabulary id; the keys are
+// unique) is the number of larger keys in its own list, plus the length of
+// the list above for a key inside the range; the keys are spread over many
+// CTAs, so no single SM sorts a row. A row whose range still holds more than
+// kCap keys after the last histogram is finished by the collection kernel's
+// first CTA of the row alone, with the remaining passes over the whole row.
 constexpr int kMsThreads = 1024;
 constexpr int kMsPasses = 2;      // histograms; later digits in the fallback
 constexpr int kMsStateInts = 32;  // per-row ranges and counters, then the histograms
 constexpr int kMsRowInts = kMsStateInts + kMsPasses * kBins;
-// A range of at most this many keys needs no further histogram: the last
-// CTA of the collection then sorts about k + kMsDone keys.
+// A range of at most this many keys needs no further histogram: the rank
+// kernel then places about k + kMsDone keys.
 constexpr int kMsDone = 512;
 static_assert(kBins == 1 << kSelectHistBits && kDigit == kSelectHistBits, "digit width");
 // The histograms' digits lie in the score's order bits (the key's top 32), so
