@@ -24,12 +24,12 @@ cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int
 
 // K4 (CUDA cores): fused tile scores + per-tile top-k_tile, no score writeback.
 // For M <= kLocalGemvMaxM and tiles of 32..256 rows dividing 256 (k_tile <= 8,
-// r = 256) it runs the warp-per-row GEMV kernel.
+// r = 256 or 512) it runs the warp-per-row GEMV kernel.
 constexpr int kLocalGemvMaxM = 2;
 bool local_topk_gemv_supported(int M, int r, int T, int k_tile);
 // The same GEMV kernel writing every score to S (M x n fp32 by position)
 // instead of selecting: the global path's writeback for one or two hidden
-// vectors at r = 256. hist0 != nullptr: it also adds the counts of the
+// vectors at r = 256 or 512. hist0 != nullptr: it also adds the counts of the
 // scores' top kSelectHistBits order bits of hidden vector m into
 // hist0 + m * hist0_stride (kSelectHistBins ints; the multi-CTA selection's
 // first histogram).

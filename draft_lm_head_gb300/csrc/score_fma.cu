@@ -160,11 +160,11 @@ local_topk_fma_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u
 // One or two hidden vectors with tiles of 32-256 rows that divide 256: the
 // contraction is a GEMV (one or two FLOP per byte of A), so CUDA cores keep
 // pace with HBM and the tensor-core kernel's machinery (TMA ring, MMA issue,
-// TMEM) only adds latency. A warp scores eight rows at a time, each lane
-// reading one 16-byte piece of every row (r = 256: coalesced 512-byte
-// requests), the first eight rows requested before waiting for u (u comes
-// from the projection kernel, A does not); the lane's share of u sits in
-// registers and a warp reduction gives each row's score. The CTA's 256 rows hold 256 / T whole tiles; each
+// TMEM) only adds latency. A warp scores eight rows at a time at r = 256 (four
+// at r = 512), each lane reading one (two) 16-byte pieces of every row
+// (coalesced 512-byte requests), the first rows requested before waiting for u
+// (u comes from the projection kernel, A does not); the lane's share of u
+// sits in registers and a warp reduction gives each row's score. The CTA's 256 rows hold 256 / T whole tiles; each
 // tile's top k_tile per hidden vector comes from one warp: every lane keeps a
 // sorted register list of its strided share of the tile's scores, then
 // k_tile rounds of a warp arg-best over the list heads (score descending,
@@ -179,7 +179,9 @@ __device__ __forceinline__ bool gemv_beats(float sa, int32_t ia, float sb, int32
 // (more registers, so fewer CTAs per SM).
 // WB: write the scores to S (M x n by position: the global path's score
 // writeback) instead of selecting.
-template <int MB, int KT, bool DB, bool WB = false>
+// P: 16-byte pieces of a row per lane (r = 256 P): a batch is 8 / P rows, so
+// a lane keeps eight loads in flight at either rank.
+template <int MB, int KT, bool DB, bool WB = false, int P = 1>
 __global__ void __launch_bounds__(kGemvThreads, DB ? (MB == 1 ? 3 : 2) : (MB == 1 ? 4 : 3))
 local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u,
                        const int32_t* __restrict__ token_ids, int64_t n, int r, int M, int T,
@@ -197,21 +199,22 @@ local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ 
     if (hist0)
       for (int i = tid; i < MB * kSelectHistBins; i += kGemvThreads) hh[i] = 0u;
   }
-  constexpr int kRows = 8;  // rows per batch and warp (loads in flight)
+  constexpr int kRows = 8 / P;  // rows per batch and warp (8 loads in flight per lane)
   {
     const int64_t pos = row0 + tid;
     svid[tid] = pos < n ? (token_ids ? __ldg(token_ids + pos) : (int32_t)pos) : 0x7FFFFFFF;
   }
-  // warp w scores rows w, w + 8, ... of the CTA's 256; lane L reads piece L
-  // of a row (r = 256: coalesced 512-byte requests)
+  // warp w scores rows w, w + 8, ... of the CTA's 256; lane L reads pieces
+  // L, L + 32, ... of a row (coalesced 512-byte requests)
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4 a[kRows];
+  uint4 a[kRows * P];
   auto load_batch = [&](int bt) {
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {
       const int64_t pos = row0 + (int64_t)(bt * kRows + i) * 8 + warp;
       const uint4* arow = reinterpret_cast<const uint4*>(A + (size_t)(pos < n ? pos : 0) * r);
-      a[i] = pos < n ? ldg_nc_v4(arow + lane) : zero;
+#pragma unroll
+      for (int q = 0; q < P; ++q) a[i * P + q] = pos < n ? ldg_nc_v4(arow + lane + 32 * q) : zero;
     }
   };
   load_batch(0);  // A before waiting for u
@@ -219,30 +222,38 @@ local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ 
   // the gather may launch once every thread has triggered, which is after
   // the projection kernel (that zeroes the ready counters) completed
   pdl_trigger();
-  float uf[MB][8];
+  float uf[MB][8 * P];
 #pragma unroll
   for (int mm = 0; mm < MB; ++mm) {
-    uint4 uv = zero;
-    if (mm < mb) uv = *reinterpret_cast<const uint4*>(u + (size_t)(m0 + mm) * r + lane * 8);
-    unpack8(uv, uf[mm]);
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      uint4 uv = zero;
+      if (mm < mb)
+        uv = *reinterpret_cast<const uint4*>(u + (size_t)(m0 + mm) * r + (lane + 32 * q) * 8);
+      unpack8(uv, uf[mm] + 8 * q);
+    }
   }
-  constexpr int kBatches = kGemvThreads / 8 / kRows;  // 4 batches of 8 rows per warp
+  constexpr int kBatches = kGemvThreads / 8 / kRows;  // batches of kRows rows per warp
   for (int bt = 0; bt < kBatches; ++bt) {
     if (!DB && bt > 0) load_batch(bt);
-    uint4 cur[kRows];  // this batch; with DB the next one is requested before it is used
+    uint4 cur[kRows * P];  // this batch; with DB the next one is requested before it is used
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) cur[i] = a[i];
+    for (int i = 0; i < kRows * P; ++i) cur[i] = a[i];
     if (DB && bt + 1 < kBatches) load_batch(bt + 1);
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {
       float part[MB];
-      float f[8];
-      unpack8(cur[i], f);
 #pragma unroll
-      for (int mm = 0; mm < MB; ++mm) {
-        part[mm] = 0.f;
+      for (int mm = 0; mm < MB; ++mm) part[mm] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) part[mm] = fmaf(f[e], uf[mm][e], part[mm]);
+      for (int q = 0; q < P; ++q) {
+        float f[8];
+        unpack8(cur[i * P + q], f);
+#pragma unroll
+        for (int mm = 0; mm < MB; ++mm) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) part[mm] = fmaf(f[e], uf[mm][8 * q + e], part[mm]);
+        }
       }
       const int rl = (bt * kRows + i) * 8 + warp;  // row within the CTA
       const bool live = row0 + rl < n;
@@ -341,14 +352,16 @@ cudaError_t launch_gemv_mb(const bf16_t* A, const bf16_t* u, const int32_t* toke
                            int r, int M, int T, int k_tile, int K, int32_t* out_ids,
                            float* out_scores, cudaStream_t s, int* ready) {
   dim3 grid((unsigned)((n + kGemvThreads - 1) / kGemvThreads), (unsigned)((M + MB - 1) / MB));
-#define GV(KT)                                                                                \
-  return launch_kernel(true, local_topk_gemv_kernel<MB, KT, DB>, grid, dim3(kGemvThreads), 0, s, \
-                       A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, ready,  \
+#define GV(KT, P)                                                                                \
+  return launch_kernel(true, local_topk_gemv_kernel<MB, KT, DB, false, P>, grid, dim3(kGemvThreads), \
+                       0, s, A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, ready,   \
                        (float*)nullptr, (int*)nullptr, 0);
-  if (k_tile <= 1) GV(1);
-  if (k_tile <= 2) GV(2);
-  if (k_tile <= 4) GV(4);
-  GV(8);
+#define GVR(KT) do { if (r == 512) GV(KT, 2); GV(KT, 1); } while (0)
+  if (k_tile <= 1) GVR(1);
+  if (k_tile <= 2) GVR(2);
+  if (k_tile <= 4) GVR(4);
+  GVR(8);
+#undef GVR
 #undef GV
 }
 
@@ -368,18 +381,21 @@ cudaError_t launch_scores_gemv(const bf16_t* A, const bf16_t* u, int64_t n, int 
                                cudaStream_t s, int* hist0, int hist0_stride) {
   if (!local_topk_gemv_supported(M, r, kGemvThreads, 1)) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)((n + kGemvThreads - 1) / kGemvThreads), 1);
-  if (M <= 1)
-    return launch_kernel(true, local_topk_gemv_kernel<1, 1, false, true>, grid, dim3(kGemvThreads),
-                         0, s, A, u, (const int32_t*)nullptr, n, r, M, kGemvThreads, 1, 0,
-                         (int32_t*)nullptr, (float*)nullptr, (int*)nullptr, S, hist0,
-                         hist0_stride);
-  return launch_kernel(true, local_topk_gemv_kernel<2, 1, true, true>, grid, dim3(kGemvThreads), 0,
-                       s, A, u, (const int32_t*)nullptr, n, r, M, kGemvThreads, 1, 0,
-                       (int32_t*)nullptr, (float*)nullptr, (int*)nullptr, S, hist0, hist0_stride);
+#define WBK(MB, DB, P)                                                                          \
+  return launch_kernel(true, local_topk_gemv_kernel<MB, 1, DB, true, P>, grid, dim3(kGemvThreads), \
+                       0, s, A, u, (const int32_t*)nullptr, n, r, M, kGemvThreads, 1, 0,           \
+                       (int32_t*)nullptr, (float*)nullptr, (int*)nullptr, S, hist0, hist0_stride)
+  if (M <= 1) {
+    if (r == 512) WBK(1, false, 2);
+    WBK(1, false, 1);
+  }
+  if (r == 512) WBK(2, true, 2);
+  WBK(2, true, 1);
+#undef WBK
 }
 
 bool local_topk_gemv_supported(int M, int r, int T, int k_tile) {
-  return gemv_enabled() && M <= kLocalGemvMaxM && r == 256 && T >= 32 &&
+  return gemv_enabled() && M <= kLocalGemvMaxM && (r == 256 || r == 512) && T >= 32 &&
          T <= kGemvThreads && kGemvThreads % T == 0 && k_tile <= 8;
 }
 

@@ -207,6 +207,29 @@ def test_two_stage_gemv_scoring(L, M, T, k):
     assert L.last_device_error() == 0
 
 
+@pytest.mark.parametrize("M", [1, 2])
+def test_gemv_scoring_rank_512(L, M):
+    # r = 512 on the CUDA-core GEMV kernel (two 16-byte pieces of a row per
+    # lane, four rows a batch): local two-stage calls over a few tile sizes,
+    # and the global route on rows long enough for the several-CTA selection
+    # (the GEMV writeback counts its first histogram)
+    case = make_case(9001, 520, 512, M, seed=29, plain_h=True)
+    W, A, B, h, tok = _dev(case)
+    _, S, h64, SL = oracle_scores(case, with_slack=True)
+    for T, k in ((256, 2), (64, 4)):
+        ids, lg, q = L.two_stage(L.LOCAL, W, A, B, h, tok, T, k, temperature=0.7)
+        ids = host(ids)
+        P.check_ids("local", ids, S, case["tok"], T, k, slack_pos=SL)
+        ex = P.exact_logits(case["W"], h64, ids)
+        P.check_logits(host(lg), ex)
+        P.check_q(host(q), ex, 0.7)
+    for C in (1, 1000):
+        ids, sc = L.lowrank_score_topk(L.GLOBAL, A, B, h, tok, C, with_scores=True)
+        P.check_ids("global", host(ids), S, case["tok"], C, slack_pos=SL)
+        P.check_order("global", host(ids), host(sc), C, 0, case["n"])
+    assert L.last_device_error() == 0
+
+
 def test_two_stage_identity_token_ids(L):
     case = make_case(1024, 64, 16, 2, seed=14, shuffle=False)
     W, A, B, h, _ = _dev(case)
