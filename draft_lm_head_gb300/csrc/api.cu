@@ -227,7 +227,7 @@ int run_select(int mode, const bf16_t* A, const bf16_t* B, const bf16_t* h,
   // tensor-core row products
   // (the GEMV form also counts the multi-CTA selection's first histogram)
   float* S = reinterpret_cast<float*>(ws + L.scores);
-  const bool gemv = local_topk_gemv_supported(M, r, 256, 1);
+  const bool gemv = scores_gemv_supported(M, r);
   int* ms_zero = L.ms ? tickets + L.ms_at : nullptr;
   e = gemv ? launch_scores_gemv(A, u, n, r, M, S, s,
                                 ms_zero ? ms_zero + row_select_multi_hist0(0) : nullptr,

@@ -24,9 +24,14 @@ cudaError_t launch_project_u(const bf16_t* B, const bf16_t* h, int d, int r, int
 
 // K4 (CUDA cores): fused tile scores + per-tile top-k_tile, no score writeback.
 // For M <= kLocalGemvMaxM and tiles of 32..256 rows dividing 256 (k_tile <= 8,
-// r = 256 or 512) it runs the warp-per-row GEMV kernel.
-constexpr int kLocalGemvMaxM = 2;
+// r = 256 or 512) it runs the warp-per-row GEMV kernel (measured faster than
+// the tensor-core kernel up to four hidden vectors; at five to eight the
+// GEMV's registers leave too few warps per SM).
+constexpr int kLocalGemvMaxM = 4;  // compiled up to; gemv_max_m() is the limit in use
+int gemv_max_m();
 bool local_topk_gemv_supported(int M, int r, int T, int k_tile);
+// The GEMV score writeback (below): one or two hidden vectors.
+bool scores_gemv_supported(int M, int r);
 // The same GEMV kernel writing every score to S (M x n fp32 by position)
 // instead of selecting: the global path's writeback for one or two hidden
 // vectors at r = 256 or 512. hist0 != nullptr: it also adds the counts of the

@@ -182,7 +182,8 @@ __device__ __forceinline__ bool gemv_beats(float sa, int32_t ia, float sb, int32
 // P: 16-byte pieces of a row per lane (r = 256 P): a batch is 8 / P rows, so
 // a lane keeps eight loads in flight at either rank.
 template <int MB, int KT, bool DB, bool WB = false, int P = 1>
-__global__ void __launch_bounds__(kGemvThreads, DB ? (MB == 1 ? 3 : 2) : (MB == 1 ? 4 : 3))
+__global__ void __launch_bounds__(kGemvThreads,
+                                  DB ? (MB == 1 ? 3 : 2) : (MB == 1 ? 4 : (MB == 2 ? 3 : 2)))
 local_topk_gemv_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u,
                        const int32_t* __restrict__ token_ids, int64_t n, int r, int M, int T,
                        int k_tile, int K, int32_t* __restrict__ out_ids,
@@ -379,7 +380,7 @@ bool gemv_enabled() {
 
 cudaError_t launch_scores_gemv(const bf16_t* A, const bf16_t* u, int64_t n, int r, int M, float* S,
                                cudaStream_t s, int* hist0, int hist0_stride) {
-  if (!local_topk_gemv_supported(M, r, kGemvThreads, 1)) return cudaErrorInvalidValue;
+  if (!scores_gemv_supported(M, r)) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)((n + kGemvThreads - 1) / kGemvThreads), 1);
 #define WBK(MB, DB, P)                                                                          \
   return launch_kernel(true, local_topk_gemv_kernel<MB, 1, DB, true, P>, grid, dim3(kGemvThreads), \
@@ -394,8 +395,25 @@ cudaError_t launch_scores_gemv(const bf16_t* A, const bf16_t* u, int64_t n, int 
 #undef WBK
 }
 
+// LMHEAD_GEMV_MAX_M = m (0..4) moves the hand-over to the tensor cores
+// (measurements only).
+int gemv_max_m() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("LMHEAD_GEMV_MAX_M");
+    v = e ? atoi(e) : kLocalGemvMaxM;
+    if (v < 0) v = 0;
+    if (v > kLocalGemvMaxM) v = kLocalGemvMaxM;
+  }
+  return v;
+}
+
+bool scores_gemv_supported(int M, int r) {
+  return gemv_enabled() && M <= 2 && (r == 256 || r == 512);
+}
+
 bool local_topk_gemv_supported(int M, int r, int T, int k_tile) {
-  return gemv_enabled() && M <= kLocalGemvMaxM && (r == 256 || r == 512) && T >= 32 &&
+  return gemv_enabled() && M <= gemv_max_m() && (r == 256 || r == 512) && T >= 32 &&
          T <= kGemvThreads && kGemvThreads % T == 0 && k_tile <= 8;
 }
 
@@ -411,8 +429,14 @@ cudaError_t launch_local_topk_fma(const bf16_t* A, const bf16_t* u, const int32_
     if (M <= 1)
       return launch_gemv_mb<1, false>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores,
                                       s, ready);
-    return launch_gemv_mb<2, true>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores, s,
-                                   ready);
+    if (M <= 2)
+      return launch_gemv_mb<2, true>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores,
+                                     s, ready);
+    // three or four: 128 registers, two CTAs per SM (measured: the call
+    // 45.0 -> 40.9 us at three, 46.7 -> 42.9 at four, the wide head at four
+    // 87.9 -> 70.7 us)
+    return launch_gemv_mb<4, false>(A, u, token_ids, n, r, M, T, k_tile, K, out_ids, out_scores,
+                                    s, ready);
   }
   // the kernel also has ~13 KB of static shared memory, so the opt-in is
   // needed below 48 KB of dynamic memory too: always raise the limit (cached)

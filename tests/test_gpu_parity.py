@@ -189,10 +189,11 @@ def test_two_stage(L, mode, C, k, temp):
 
 
 @pytest.mark.parametrize("T,k", [(256, 2), (64, 8), (32, 1)])
-@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
 def test_two_stage_gemv_scoring(L, M, T, k):
-    # one or two hidden vectors at r = 256 take the CUDA-core scoring kernel
-    # (tiles of 32-256 rows in one 256-row CTA). d = 264: W rows and h end off
+    # up to four hidden vectors at r = 256 take the CUDA-core scoring kernel
+    # (tiles of 32-256 rows in one 256-row CTA; one, two or four vectors per
+    # CTA). d = 264: W rows and h end off
     # a 256-element step; n = 5003: the last tile is partial and the last CTA
     # holds tile slots past n.
     case = make_case(5003, 264, 256, M, seed=23, plain_h=True)
@@ -207,7 +208,7 @@ def test_two_stage_gemv_scoring(L, M, T, k):
     assert L.last_device_error() == 0
 
 
-@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("M", [1, 2, 4])
 def test_gemv_scoring_rank_512(L, M):
     # r = 512 on the CUDA-core GEMV kernel (two 16-byte pieces of a row per
     # lane, four rows a batch): local two-stage calls over a few tile sizes,
