@@ -403,7 +403,7 @@ int gemv_max_m() {
     const char* e = getenv("LMHEAD_GEMV_MAX_M");
     v = e ? atoi(e) : kLocalGemvMaxM;
     if (v < 0) v = 0;
-    if (v > kLocalGemvMaxM) v = kLocalGemvMaxM;
+    if (v > 8) v = 8;  // five to eight: two grid rows of four (A streamed twice)
   }
   return v;
 }
