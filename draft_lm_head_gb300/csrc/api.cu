@@ -55,7 +55,7 @@ struct Layout {
   bool ms = false;  // global Top-C through several CTAs per row
 };
 
-// The fused scoring kernel of local mode: one or two hidden vectors take the
+// The fused scoring kernel of local mode: up to four hidden vectors take the
 // warp-per-row GEMV kernel, more the tensor cores, where each applies.
 bool use_tc(int mode, int r, int T, int k_tile, int M) {
   return mode == LMHEAD_LOCAL && local_topk_tc_supported(r, T, k_tile) &&

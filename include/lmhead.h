@@ -208,7 +208,7 @@ int lmhead_pruned_head(const lmhead_bf16* W_pruned, const lmhead_bf16* h, int n_
  * with no device allocator of its own. Arguments, outputs and results are
  * those of lmhead_two_stage with mode = LMHEAD_LOCAL, C_or_tile = T.
  *   Speed: it scores as lmhead_two_stage does (the warp-per-row GEMV kernel
- *   for one or two hidden vectors at r = 256 or 512, the tensor-core kernel for
+ *   for up to four hidden vectors at r = 256 or 512, the tensor-core kernel for
  *   tiles of a multiple of 128 rows), except that tiles of other sizes score
  *   on the CUDA-core tile kernel (the tensor-core form for them needs scratch
  *   that grows with M and n), and the gather never overlaps the scoring
