@@ -157,15 +157,16 @@ local_topk_fma_kernel(const bf16_t* __restrict__ A, const bf16_t* __restrict__ u
 }
 
 // ---------------------------------------------------------------- K4 (gemv)
-// One or two hidden vectors with tiles of 32-256 rows that divide 256: the
-// contraction is a GEMV (one or two FLOP per byte of A), so CUDA cores keep
+// Up to four hidden vectors with tiles of 32-256 rows that divide 256: the
+// contraction is a GEMV (one to four FLOP per byte of A), so CUDA cores keep
 // pace with HBM and the tensor-core kernel's machinery (TMA ring, MMA issue,
 // TMEM) only adds latency. A warp scores eight rows at a time at r = 256 (four
 // at r = 512), each lane reading one (two) 16-byte pieces of every row
 // (coalesced 512-byte requests), the first rows requested before waiting for u
 // (u comes from the projection kernel, A does not); the lane's share of u
-// sits in registers and a warp reduction gives each row's score. The CTA's 256 rows hold 256 / T whole tiles; each
-// tile's top k_tile per hidden vector comes from one warp: every lane keeps a
+// sits in registers and a warp reduction gives each row's score. The CTA's
+// 256 rows hold 256 / T whole tiles; each tile's top k_tile per hidden vector
+// comes from one warp: every lane keeps a
 // sorted register list of its strided share of the tile's scores, then
 // k_tile rounds of a warp arg-best over the list heads (score descending,
 // then the smaller vocabulary id).
