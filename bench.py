@@ -368,6 +368,59 @@ def time_noalloc(torch, L, head, rot_h, hbm, reps=40):
     return res
 
 
+def time_shards(torch, L, head, hbm, M=64, shard_counts=(2, 4), reps=40):
+    """The vocabulary-sharded local head on one GPU: for G shards of whole
+    tiles (the headline head, M hidden vectors), each shard's call (selection
+    and gather over its own rows, then the softmax from all shards' row stats)
+    replayed alone in a graph. The slowest shard is what every GPU of a G-GPU
+    call would spend, before the 8-byte-per-row all-gather of the stats."""
+    from draft_lm_head_gb300 import shard as SH
+    n, d = head["W"].shape
+    r = head["B"].shape[0]
+    T, k = WORKLOAD.T, WORKLOAD.k_tile
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    B = dev(head["B"])
+    h = dev(hidden(head["W"], M, 0))
+    res = []
+    for G in shard_counts:
+        per = []
+        for (p0, p1) in SH.shard_ranges(n, T, G):
+            Ws, As, toks, rowmap = SH.shard_inputs(head["W"], head["A"], head["tok"], p0, p1)
+            Ws, As = dev(Ws), dev(As)
+            toks = torch.from_numpy(toks).cuda()
+            rowmap = torch.from_numpy(rowmap).cuda()
+            K = L.candidate_count(L.LOCAL, p1 - p0, T, k)
+            out = (torch.empty((M, K), dtype=torch.int32, device="cuda"),
+                   torch.empty((M, K), dtype=torch.float32, device="cuda"),
+                   torch.empty((M, 2), dtype=torch.float32, device="cuda"))
+            q = torch.empty((M, K), dtype=torch.float32, device="cuda")
+            all_stats = torch.ones((G, M, 2), dtype=torch.float32, device="cuda")
+            ws = L.Workspace()
+
+            def call():
+                L.shard_two_stage(Ws, As, B, h, toks, rowmap, T, k, workspace=ws, out=out)
+                L.shard_softmax(all_stats, out[1], out=q)
+
+            gr = make_graph(torch, call)
+            gr.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                gr.replay()
+            b.record()
+            torch.cuda.synchronize()
+            per.append(round(a.elapsed_time(b) * 1e3 / reps, 2))
+            del gr, Ws, As
+        res.append({"shards": G, "M": M, "shard_us": per, "slowest_us": max(per),
+                    "note": "each shard alone on one GPU, its W rows resident (one copy)"})
+        torch.cuda.empty_cache()
+    return res
+
+
 def time_cluster(torch, L, head, rot_h, hbm, group=128, G=8, reps=40):
     """Graph-replayed timings of the cluster-level route on the same head (A
     in vocabulary order, groups of `group` consecutive rows, the G best groups
@@ -844,10 +897,15 @@ def run_ours(args):
     after_q = {}
     cluster = []
     noalloc = []
+    shards = []
     if not args.no_sweep and rank == 0:
         after_q = time_after_q(torch, L, outs[0], hbm)
         cluster = time_cluster(torch, L, head, rot, hbm)
         noalloc = time_noalloc(torch, L, head, rot, hbm)
+        try:
+            shards = time_shards(torch, L, head, hbm)
+        except Exception as exc:  # a side measurement: report it, keep the line
+            shards = [{"error": f"{type(exc).__name__}: {exc}"}]
     configs = []
     if not args.no_configs and rank == 0:
         configs = time_configs(torch, L, hbm)
@@ -876,7 +934,7 @@ def run_ours(args):
             "step_hbm_frac": round(step_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm, 4),
             "unique_rows": U, "latency_us": lat, "parity_counts": parity, "sweep": sweep,
             "configs": configs, "vs_dense": dense_speedups(configs), "after_q": after_q,
-            "cluster_route": cluster, "noalloc": noalloc,
+            "cluster_route": cluster, "noalloc": noalloc, "sharded": shards,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
